@@ -1,0 +1,112 @@
+"""Seeded synthetic inputs for the KDA layer.
+
+This module only draws random numbers; it holds none of the layer's arithmetic.
+Both the GPU path and the float64 oracle read the exact bytes it produces.
+
+Recipe (the value distributions of the layer's serving workloads):
+  q, k ~ N(0, 1) per element, each [d_k] vector L2-normalised in float64, then
+         rounded to the storage dtype (bf16 or fp32);
+  v    ~ N(0, 1), rounded to the storage dtype;
+  beta  = sigmoid(N(0, 1)) in fp32 (one per token and head);
+  alpha = exp(-softplus(N(0, 1) + 2)) in fp32 per channel ("config" decay), or
+          exp(-softplus(N(0, 1) - 5)) ("mild" decay: alpha near 1, so a state
+          carried across many chunks still matters);
+  decode states ~ N(0, 0.05^2) fp32.
+
+Every sequence draws from its own stream, ``torch.Generator`` seeded with
+``seed * 1000003 + seq``, in fixed blocks of 4096 tokens (q, k, v, alpha, beta in
+that order per block), so any batch can be generated piecewise and a sequence's
+values do not depend on the other sequences of its batch.
+"""
+import numpy as np
+import torch
+
+BLOCK = 4096
+_DECAY_SHIFT = {"config": 2.0, "mild": -5.0}
+
+
+def _stream(seed: int, seq: int) -> torch.Generator:
+    g = torch.Generator()
+    g.manual_seed(int(seed) * 1000003 + int(seq))
+    return g
+
+
+def _unit_rows(x: torch.Tensor) -> torch.Tensor:
+    return x / torch.linalg.vector_norm(x, dim=-1, keepdim=True)
+
+
+def gen_sequence_block(g, n, H, d_k, d_v, decay):
+    """One block of n tokens from generator g, all float64."""
+    q = _unit_rows(torch.randn((n, H, d_k), generator=g, dtype=torch.float64))
+    k = _unit_rows(torch.randn((n, H, d_k), generator=g, dtype=torch.float64))
+    v = torch.randn((n, H, d_v), generator=g, dtype=torch.float64)
+    shift = _DECAY_SHIFT[decay]
+    alpha = torch.exp(-torch.nn.functional.softplus(
+        torch.randn((n, H, d_k), generator=g, dtype=torch.float64) + shift))
+    beta = torch.sigmoid(torch.randn((n, H), generator=g, dtype=torch.float64))
+    return q, k, v, alpha, beta
+
+
+def gen_prefill(seq_lens, H, d_k, d_v, seed, dtype=torch.bfloat16, decay="config",
+                pin=False):
+    """Packed prefill inputs on the host.
+
+    Returns dict with q, k [T, H, d_k] and v [T, H, d_v] in ``dtype``, alpha
+    [T, H, d_k] and beta [T, H] in fp32, cu_seqlens int32 [n+1] and seq_lens.
+    ``seq_lens[i]`` tokens are drawn for sequence i from its own stream.
+    """
+    seq_lens = [int(x) for x in seq_lens]
+    T = sum(seq_lens)
+    kw = {"pin_memory": True} if pin else {}
+    q = torch.empty((T, H, d_k), dtype=dtype, **kw)
+    k = torch.empty((T, H, d_k), dtype=dtype, **kw)
+    v = torch.empty((T, H, d_v), dtype=dtype, **kw)
+    alpha = torch.empty((T, H, d_k), dtype=torch.float32, **kw)
+    beta = torch.empty((T, H), dtype=torch.float32, **kw)
+    off = 0
+    for s, L in enumerate(seq_lens):
+        g = _stream(seed, s)
+        for b in range(0, L, BLOCK):
+            n = min(BLOCK, L - b)
+            qb, kb, vb, ab, bb = gen_sequence_block(g, BLOCK, H, d_k, d_v, decay)
+            sl = slice(off + b, off + b + n)
+            q[sl] = qb[:n].to(dtype)
+            k[sl] = kb[:n].to(dtype)
+            v[sl] = vb[:n].to(dtype)
+            alpha[sl] = ab[:n].to(torch.float32)
+            beta[sl] = bb[:n].to(torch.float32)
+        off += L
+    cu = torch.zeros(len(seq_lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.tensor(np.cumsum(seq_lens), dtype=torch.int32) if seq_lens else cu[1:]
+    return {"q": q, "k": k, "v": v, "alpha": alpha, "beta": beta,
+            "cu_seqlens": cu, "seq_lens": seq_lens}
+
+
+def gen_decode(n_seqs, H, d_k, d_v, seed, step, dtype=torch.bfloat16, decay="config"):
+    """Inputs of one batched decode step: one token per sequence.
+
+    Sequence i of step ``step`` draws from stream (seed + 7919 * (step + 1), i).
+    Returns q, k [n, H, d_k], v [n, H, d_v] in ``dtype``; alpha [n, H, d_k] and
+    beta [n, H] fp32.
+    """
+    q = torch.empty((n_seqs, H, d_k), dtype=dtype)
+    k = torch.empty((n_seqs, H, d_k), dtype=dtype)
+    v = torch.empty((n_seqs, H, d_v), dtype=dtype)
+    alpha = torch.empty((n_seqs, H, d_k), dtype=torch.float32)
+    beta = torch.empty((n_seqs, H), dtype=torch.float32)
+    # one generator per step; sequences take consecutive rows of its block
+    g = _stream(seed + 7919 * (step + 1), 0)
+    qb, kb, vb, ab, bb = gen_sequence_block(g, n_seqs, H, d_k, d_v, decay)
+    q[:] = qb.to(dtype)
+    k[:] = kb.to(dtype)
+    v[:] = vb.to(dtype)
+    alpha[:] = ab.to(torch.float32)
+    beta[:] = bb.to(torch.float32)
+    return {"q": q, "k": k, "v": v, "alpha": alpha, "beta": beta}
+
+
+def gen_states(n, H, d_k, d_v, seed, std=0.05):
+    """fp32 states [n, H, d_k, d_v] with N(0, std^2) entries."""
+    g = _stream(seed, 999_999_937)
+    return (torch.randn((n, H, d_k, d_v), generator=g, dtype=torch.float64) * std).to(
+        torch.float32)

@@ -1,0 +1,28 @@
+"""Float64 CPU oracle of the KDA (Kimi Delta Attention) layer.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code with
+the GPU library and never calls it; the GPU library never imports it.
+
+Contents
+--------
+``run``            token-by-token float64 recurrence (C, OpenMP) over a packed
+                   variable-length batch, with snapshots and resume
+                   ("Kimi K3 Tech Intro", sections 2.1-2.3).
+``chunked``        the chunked (block-matrix) form in float64 numpy, written from
+                   the recurrence alone; used to check that blocking the
+                   sequence into chunks of any size changes nothing
+                   (the block-matrix form of the yunthe.com "Kimi K3 open-source
+                   practice" page, FlashKDA paragraph).
+``snapshot_positions`` / ``reusable_prefix``
+                   which absolute positions carry snapshots, and how much of a
+                   shared prefix a snapshot grid lets a request reuse
+                   ("Kimi K3 Tech Intro", sections 2.1-2.2).
+``window_bound``   a rigorous upper bound on how much a state that is forgotten
+                   at the start of a window can change the states inside it,
+                   used to check long sequences on sampled windows.
+"""
+from .recurrent import run, threads, DT_BF16, DT_F32, DT_F64  # noqa: F401
+from .chunked import chunked  # noqa: F401
+from .positions import snapshot_positions, reusable_prefix  # noqa: F401
+from .bounds import window_bound, state_norm_bound  # noqa: F401
