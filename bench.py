@@ -1,0 +1,472 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA layer's hot path on GB300: chunked prefill tokens/s and
+decode-step HBM GB/s, each against the measured roofline, with the float64 CPU
+oracle timed on the host cores beside it.
+
+One step = one chunked prefill of the 4 x 8192-token, 32-head, d = 128 bf16
+batch (gate products, chunk-local products, the fp32 state carry, outputs and a
+state snapshot every 256 tokens into the block-indexed pool).  The decode step
+(512 sequences x 32 heads, one token each, fp32 states updated in place) and the
+snapshot gather/restore copies are timed in the same run and reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 launch one process per GPU with torch.distributed.run; each rank runs
+its own replica (the layer has no cross-device exchange), value = all ranks'
+tokens / the slowest rank's time.  Rank 0 prints one JSON line.
+"""
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "KDA prefill tokens/s (% bf16 TC peak) and decode-step HBM GB/s (% of 8 TB/s)"
+PREFILL_CFG = "prefill_4x8k"
+DECODE_CFG = "decode_512x32"
+
+# Algorithmic traffic and work per token-head of the prefill (d_k = d_v = 128,
+# chunk 64, snapshot every 256 tokens):
+#   bytes: q, k, v bf16 (3 x 256) + alpha fp32 (512) + beta (4) + o bf16 (256)
+#          + one 64 KiB fp32 snapshot per 256 tokens (256)            = 1796 B
+#   flops: 6 d_k d_v (state products) + C (3 d_k + 2 d_v) (chunk-local) = 139264
+PREFILL_BYTES_PER_TH = 3 * 256 + 512 + 4 + 256 + 256
+PREFILL_FLOPS_PER_TH = 6 * 128 * 128 + 64 * (3 * 128 + 2 * 128)
+
+
+def decode_bytes(n, H, d):
+    """State read + write (fp32) plus the token's q, k, v (bf16), alpha (fp32),
+    beta (fp32) and o (bf16)."""
+    return 2 * n * H * d * d * 4 + n * H * (3 * d * 2 + d * 4 + 4 + d * 2)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a timed region."""
+
+    def __init__(self, device):
+        self.proc = None
+        self.path = None
+        try:
+            bus = torch.cuda.get_device_properties(device).pci_bus_id
+        except Exception:
+            bus = None
+        self.sel = ["-i", bus] if bus else []
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *self.sel, f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        with open(self.path) as f:
+            rows = list(csv.reader(io.StringIO(f.read())))
+        os.unlink(self.path)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1].strip().split()[0]))
+                smax.append(float(r[2].strip().split()[0]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def kernel_fingerprint():
+    """Hash of the CUDA sources, to tie recorded ncu traffic to the kernel it measured."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "hybrid_linear_attention_kda_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# DRAM bytes per launch of the dominant prefill kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the source fingerprint
+# it was taken on; any other fingerprint reports null.
+RECORDED_TRAFFIC = {}
+
+
+def barrier(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x, dist_on, dev):
+    if not dist_on:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_prefill_sample(data, seconds_target=10.0):
+    """Time the float64 oracle on a bounded sample of the prefill workload: the
+    first n tokens of every sequence, all heads, n sized for about
+    ``seconds_target`` of CPU time.  Returns (tokens/s, cores, sample text, secs)."""
+    import oracle
+    H = data["q"].shape[1]
+    lens = data["seq_lens"]
+    n_seq = len(lens)
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+
+    def run(n_tok):
+        idx = torch.cat([torch.arange(cu[s], cu[s] + n_tok) for s in range(n_seq)])
+        sub = {key: data[key][idx] for key in ("q", "k", "v", "alpha", "beta")}
+        t0 = time.perf_counter()
+        oracle.run(sub["q"], sub["k"], sub["v"], sub["alpha"], sub["beta"],
+                   [i * n_tok for i in range(n_seq + 1)], want_final=True)
+        return time.perf_counter() - t0
+
+    cal = 64
+    t_cal = max(run(cal), 1e-3)
+    n_tok = int(min(min(lens), max(cal, cal * seconds_target / t_cal)))
+    n_tok = max(64, (n_tok // 64) * 64)
+    secs = run(n_tok)
+    tokens = n_seq * n_tok
+    sample = (f"first {n_tok} of {lens[0]} tokens of each of the {n_seq} sequences, all {H} heads "
+              f"({tokens} tokens, {secs:.1f} s)")
+    return tokens / secs, oracle.threads(), sample, secs
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def bench_ours(args, rank, world, dev, dist_on):
+    import hybrid_linear_attention_kda_gb300 as kda
+    from hybrid_linear_attention_kda_gb300 import inputs
+
+    lib = kda.load()
+    peaks = load_peaks()
+    w = inputs.WORKLOADS[PREFILL_CFG]
+    n, H, d, T = w["n_seqs"], w["H"], w["d"], w["T"]
+    host = inputs.gen_prefill([T] * n, H, d, d, w["seed"] + 1000 * rank, pin=True)
+    x = {key: host[key].to(dev) for key in ("q", "k", "v", "alpha", "beta", "cu_seqlens")}
+    total = n * T
+    n_ord = T // 256
+    pool = torch.zeros((n * n_ord, H, d, d), dtype=torch.float32, device=dev)
+    table = torch.arange(n * n_ord, dtype=torch.int32, device=dev).view(n, n_ord)
+    o = torch.empty((total, H, d), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((n, H, d, d), dtype=torch.float32, device=dev)
+    pargs = kda.make_prefill_args(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["cu_seqlens"],
+                                  total, o, pool=pool, snap_table=table, final_state=fin)
+    need = kda.kda_prefill_workspace_size(pargs)
+    ws = None
+    if need:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        pargs.workspace, pargs.workspace_bytes = ws.data_ptr(), need
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    import ctypes
+    pref = ctypes.byref(pargs)
+
+    def prefill_once():
+        st = lib.kda_prefill_chunked(pref, sh)
+        if st != 0:
+            raise RuntimeError(f"prefill failed: {kda.kda_status_string(st)}: {lib.kda_last_error()}")
+
+    warm = max(3, args.warmup)
+    for _ in range(warm):
+        prefill_once()
+    assert kda.kda_check_status(stream) == 0
+
+    # ---- device-resident timed region
+    clocks = ClockSampler(dev)
+    clocks.start()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier(dist_on)
+    launches0 = kda.kda_launch_count()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        prefill_once()
+        ev[i + 1].record(stream)
+    barrier(dist_on)
+    launches = kda.kda_launch_count() - launches0
+    clk = clocks.stop()
+    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), dist_on, dev)
+    ms_per_step = total_ms / args.steps
+    value = world * total * args.steps / (total_ms / 1e3)
+    assert kda.kda_check_status(stream) == 0
+
+    # dominant kernel: the stage timing entry point splits a step by kernel when
+    # the path has several; the token-serial path is one launch per step
+    stage = getattr(kda, "prefill_stage_times", None)
+    stages = stage(pargs, stream) if stage else {"prefill": statistics.mean(step_ms)}
+    dom_name, dom_ms = max(stages.items(), key=lambda kv: kv[1])
+    th = total * H
+    alg_bytes = th * PREFILL_BYTES_PER_TH + n * H * d * d * 4
+    alg_flops = th * PREFILL_FLOPS_PER_TH
+    fp = kernel_fingerprint()
+    traffic = RECORDED_TRAFFIC.get(fp)
+    roofline = {"bound": "hbm", "kernel": dom_name,
+                "achieved": alg_bytes / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": alg_bytes / (dom_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                "traffic": traffic, "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": alg_bytes}
+    tensor = {"achieved_tflops": alg_flops / (ms_per_step / 1e3) / 1e12,
+              "peak_tflops": peaks["bf16_tflops"],
+              "frac": alg_flops / (ms_per_step / 1e3) / 1e12 / peaks["bf16_tflops"],
+              "algorithmic_flops_per_step": alg_flops}
+
+    # ---- end to end through the C ABI from pinned host buffers
+    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    fin_host = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    h2d = sum(host[key].numel() * host[key].element_size()
+              for key in ("q", "k", "v", "alpha", "beta", "cu_seqlens"))
+    d2h = o_host.numel() * o_host.element_size() + fin_host.numel() * fin_host.element_size()
+
+    def e2e_once():
+        for key in ("q", "k", "v", "alpha", "beta", "cu_seqlens"):
+            x[key].copy_(host[key], non_blocking=True)
+        prefill_once()
+        o_host.copy_(o, non_blocking=True)
+        fin_host.copy_(fin, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_once()
+    barrier(dist_on)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_once()
+    e1.record(stream)
+    barrier(dist_on)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist_on, dev)
+    e2e = {"value": world * total * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del x, o, pool, ws
+
+    # ---- decode step, 512 x 32 heads, states updated in place
+    dw = inputs.WORKLOADS[DECODE_CFG]
+    dn, dH, dd = dw["n_seqs"], dw["H"], dw["d"]
+    dpool = inputs.gen_states(dn, dH, dd, dd, dw["seed"], std=dw["state_std"]).to(dev)
+    dslots = torch.arange(dn, dtype=torch.int32, device=dev)
+    n_sets = 8                     # rotate inputs so they do not sit in L2 between steps
+    dins = [{k_: t.to(dev) for k_, t in inputs.gen_decode(dn, dH, dd, dd, dw["seed"], s).items()}
+            for s in range(n_sets)]
+    do = torch.empty((dn, dH, dd), dtype=torch.bfloat16, device=dev)
+
+    def decode_once(i):
+        z = dins[i % n_sets]
+        kda.kda_decode_step(z["q"], z["k"], z["v"], z["alpha"], z["beta"], dpool, dslots, do,
+                            stream=stream)
+
+    for i in range(warm):
+        decode_once(i)
+    barrier(dist_on)
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d_launch0 = kda.kda_launch_count()
+    d0.record(stream)
+    for i in range(args.steps):
+        decode_once(i)
+    d1.record(stream)
+    barrier(dist_on)
+    d_launches = kda.kda_launch_count() - d_launch0
+    dec_ms = max_over_ranks(d0.elapsed_time(d1), dist_on, dev) / args.steps
+    dbytes = decode_bytes(dn, dH, dd)
+    dec_gbs = dbytes / (dec_ms / 1e3) / 1e9
+    assert kda.kda_check_status(stream) == 0
+
+    # decode end to end: per step copy the token's inputs in and the outputs out
+    dhost = [{k_: t.pin_memory() for k_, t in inputs.gen_decode(dn, dH, dd, dd, dw["seed"], s).items()}
+             for s in range(2)]
+    do_host = torch.empty(do.shape, dtype=do.dtype, pin_memory=True)
+    d_h2d = sum(t.numel() * t.element_size() for t in dhost[0].values())
+    d_d2h = do_host.numel() * do_host.element_size()
+    z = dins[0]
+
+    def decode_e2e(i):
+        for k_, t in dhost[i % 2].items():
+            z[k_].copy_(t, non_blocking=True)
+        decode_once(0)
+        do_host.copy_(do, non_blocking=True)
+
+    for i in range(2):
+        decode_e2e(i)
+    barrier(dist_on)
+    d0.record(stream)
+    for i in range(args.steps):
+        decode_e2e(i)
+    d1.record(stream)
+    barrier(dist_on)
+    dec_e2e_ms = max_over_ranks(d0.elapsed_time(d1), dist_on, dev) / args.steps
+
+    # ---- snapshot gather + restore of 128 states (64 KiB each)
+    gsl = torch.arange(0, 2 * 128, 2, dtype=torch.int32, device=dev) % dn
+    gbuf = torch.empty((128, dH, dd, dd), dtype=torch.float32, device=dev)
+    rsl = torch.arange(1, 2 * 128, 2, dtype=torch.int32, device=dev) % dn
+    for _ in range(2):
+        kda.kda_snapshot_gather(dpool, gsl, gbuf, stream=stream)
+        kda.kda_snapshot_restore(gbuf, dpool, rsl, stream=stream)
+    barrier(dist_on)
+    d0.record(stream)
+    for _ in range(args.steps):
+        kda.kda_snapshot_gather(dpool, gsl, gbuf, stream=stream)
+        kda.kda_snapshot_restore(gbuf, dpool, rsl, stream=stream)
+    d1.record(stream)
+    barrier(dist_on)
+    copy_ms = max_over_ranks(d0.elapsed_time(d1), dist_on, dev) / args.steps
+    copy_bytes = 2 * 2 * gbuf.numel() * 4
+    assert kda.kda_check_status(stream) == 0
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": warm, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), alpha=exp(-softplus(N(0,1)+2)), beta=sigmoid(N(0,1)))",
+        "config": {"workload": f"{PREFILL_CFG}: {n} sequences x {T} tokens, H={H}, d_k=d_v={d}, "
+                               "bf16 q/k/v/o, fp32 alpha/beta/state, chunk 64, snapshot every 256 "
+                               "tokens into a block-indexed pool, zero initial state",
+                   "l2": f"inputs larger than L2: {alg_bytes / 1e9:.2f} GB of algorithmic traffic per step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "tensor": tensor,
+        "stage_ms": stages,
+        "e2e": e2e,
+        "clocks": clk,
+        "gpu_launches": launches,
+        "decode": {"workload": f"{DECODE_CFG}: {dn} sequences x {dH} heads, d={dd}, one token each, "
+                               "fp32 states N(0,0.05^2) updated in place in the pool",
+                   "value": world * dec_gbs, "unit": "GB/s", "ms_per_step": dec_ms,
+                   "frac_of_8tbs": dec_gbs / 8000.0,
+                   "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm_gbs"],
+                                "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
+                                "algorithmic_bytes_per_launch": dbytes},
+                   "gpu_launches": d_launches,
+                   "e2e": {"value": world * dbytes / (dec_e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                           "ms_per_step": dec_e2e_ms, "h2d_bytes_per_step": d_h2d,
+                           "d2h_bytes_per_step": d_d2h}},
+        "snapshot_copy": {"value": copy_bytes / (copy_ms / 1e3) / 1e9, "unit": "GB/s",
+                          "ms_per_step": copy_ms, "states": 128},
+        "kernel_fingerprint": fp,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        tps, cores, sample, _ = oracle_prefill_sample(host, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    return line
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def bench_reference(args):
+    """The float64 oracle as it stands, on the host cores: each step a bounded
+    sample of the prefill workload."""
+    from hybrid_linear_attention_kda_gb300 import inputs
+    w = inputs.WORKLOADS[PREFILL_CFG]
+    host = inputs.gen_prefill([w["T"]] * w["n_seqs"], w["H"], w["d"], w["d"], w["seed"])
+    budget = max(2.0, 150.0 / (args.steps + max(3, args.warmup)))
+    times, toks = [], 0
+    warm = max(3, args.warmup)
+    sample = None
+    cores = None
+    for i in range(warm + args.steps):
+        tps, cores, sample, secs = oracle_prefill_sample(host, budget)
+        if i >= warm:
+            times.append(secs)
+            toks += tps * secs
+    value = toks / sum(times)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": warm,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{PREFILL_CFG} (bounded sample per step)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world and world == 1 and args.gpus > 1:
+        sys.exit("for --gpus > 1 launch one process per GPU with torch.distributed.run")
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(bench_reference(args)), flush=True)
+        return
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_on = world > 1
+    if dist_on:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    line = bench_ours(args, rank, world, dev, dist_on)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,282 @@
+// C-ABI entry points of libkda.so: argument checks, the device status word, and
+// dispatch to the kernels.  Declarations and the contract live in include/kda.h.
+#include <atomic>
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <thread>
+
+#include "kda_common.cuh"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+kda_status_t fail(kda_status_t st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+kda_status_t fail(kda_status_t st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+kda_status_t cuda_fail(cudaError_t e, const char* what) {
+    return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// One status word per device, in this library's own device memory.
+__device__ uint32_t g_status_word;
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices];
+std::mutex g_status_mu;
+
+// Device address of the current device's status word (looked up once per device).
+kda_status_t status_ptr(uint32_t** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(KDA_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_status_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+        g_status_ptr[dev] = static_cast<uint32_t*>(p);
+    }
+    *out = g_status_ptr[dev];
+    return KDA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kda_status_t check_dims(int32_t H, int32_t d_k, int32_t d_v, int32_t dtype) {
+    if (H <= 0) return fail(KDA_ERR_INVALID_ARG, "n_heads must be >= 1 (got %d)", H);
+    if (d_k != d_v || (d_k != 64 && d_k != 128))
+        return fail(KDA_ERR_UNSUPPORTED, "d_k == d_v in {64, 128} required (got %d, %d)", d_k, d_v);
+    if (dtype != KDA_BF16 && dtype != KDA_FP32)
+        return fail(KDA_ERR_UNSUPPORTED, "dtype %d", dtype);
+    return KDA_OK;
+}
+
+#define KDA_REQUIRE_PTR(p, name)                                                        \
+    do {                                                                                \
+        if (!(p)) return fail(KDA_ERR_INVALID_ARG, "%s is NULL", name);                 \
+        if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name); \
+    } while (0)
+
+constexpr int64_t kMaxSeqs = 1 << 20;
+
+kda_status_t validate_prefill(const kda_prefill_args* a) {
+    if (!a) return fail(KDA_ERR_INVALID_ARG, "args is NULL");
+    kda_status_t st = check_dims(a->n_heads, a->d_k, a->d_v, a->dtype);
+    if (st != KDA_OK) return st;
+    if (a->n_seqs < 0 || a->n_seqs > kMaxSeqs)
+        return fail(KDA_ERR_INVALID_ARG, "n_seqs %d outside [0, %lld]", a->n_seqs, (long long)kMaxSeqs);
+    if (a->chunk != 64) return fail(KDA_ERR_UNSUPPORTED, "chunk must be 64 (got %d)", a->chunk);
+    if (a->snap_interval != 256)
+        return fail(KDA_ERR_UNSUPPORTED, "snap_interval must be 256 (got %d)", a->snap_interval);
+    if (a->total_tokens < 0 || a->total_tokens > (int64_t)INT32_MAX)
+        return fail(KDA_ERR_INVALID_ARG, "total_tokens %lld outside [0, 2^31)", (long long)a->total_tokens);
+    if (a->reserved0 != 0) return fail(KDA_ERR_INVALID_ARG, "reserved0 must be 0");
+    if (a->n_slots < 0) return fail(KDA_ERR_INVALID_ARG, "n_slots < 0");
+    if (a->n_seqs == 0) return KDA_OK;
+    KDA_REQUIRE_PTR(a->cu_seqlens, "cu_seqlens");
+    if (a->total_tokens > 0) {
+        KDA_REQUIRE_PTR(a->q, "q");
+        KDA_REQUIRE_PTR(a->k, "k");
+        KDA_REQUIRE_PTR(a->v, "v");
+        KDA_REQUIRE_PTR(a->alpha, "alpha");
+        KDA_REQUIRE_PTR(a->beta, "beta");
+        KDA_REQUIRE_PTR(a->o, "o");
+    }
+    if (a->start_pos && !aligned16(a->start_pos)) return fail(KDA_ERR_INVALID_ARG, "start_pos misaligned");
+    if (a->init_slot || a->snap_table) {
+        KDA_REQUIRE_PTR(a->pool, "pool (needed by init_slot / snap_table)");
+        if (a->n_slots <= 0) return fail(KDA_ERR_INVALID_ARG, "n_slots must be > 0 with a pool");
+    }
+    if (a->init_slot && !aligned16(a->init_slot)) return fail(KDA_ERR_INVALID_ARG, "init_slot misaligned");
+    if (a->snap_table) {
+        if (!aligned16(a->snap_table)) return fail(KDA_ERR_INVALID_ARG, "snap_table misaligned");
+        if (a->snap_table_stride <= 0)
+            return fail(KDA_ERR_INVALID_ARG, "snap_table_stride must be > 0 with a snap_table");
+    }
+    if (a->final_state && !aligned16(a->final_state))
+        return fail(KDA_ERR_INVALID_ARG, "final_state misaligned");
+    return KDA_OK;
+}
+
+size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+// Workspace of the path the arguments select (bytes, 256-byte multiple).
+size_t workspace_bytes_for(const kda_prefill_args* a) {
+    (void)a;
+    return 0;
+}
+
+std::atomic<uint64_t> g_launches{0};
+
+}  // namespace
+
+void kda::note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+extern "C" {
+
+uint64_t kda_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+
+int32_t kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+const char* kda_status_string(kda_status_t s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_DEVICE_STATUS: return "KDA_ERR_DEVICE_STATUS";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+const char* kda_last_error(void) { return g_last_error; }
+
+size_t kda_prefill_workspace_size(const kda_prefill_args* a) {
+    if (!a || a->n_seqs < 0 || a->n_seqs > kMaxSeqs) return 0;
+    return workspace_bytes_for(a);
+}
+
+kda_status_t kda_prefill_chunked(const kda_prefill_args* a, void* stream) {
+    kda_status_t st = validate_prefill(a);
+    if (st != KDA_OK) return st;
+    if (a->n_seqs == 0) return KDA_OK;
+    const size_t need = workspace_bytes_for(a);
+    if (need > 0 && (!a->workspace || a->workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(a->workspace) & 255u)))
+        return fail(KDA_ERR_INVALID_ARG, "workspace must be >= %zu bytes and 256-byte aligned", need);
+    kda::PrefillLaunch p;
+    p.a = *a;
+    p.order = nullptr;
+    st = status_ptr(&p.status);
+    if (st != KDA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = kda::launch_prefill_token(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return KDA_OK;
+}
+
+kda_status_t kda_decode_step(int32_t n_seqs, int32_t n_heads, int32_t d_k, int32_t d_v,
+                             int32_t dtype, const void* q, const void* k, const void* v,
+                             const float* alpha, const float* beta, float* pool,
+                             int64_t n_slots, const int32_t* state_slot, void* o,
+                             float scale, void* stream) {
+    kda_status_t st = check_dims(n_heads, d_k, d_v, dtype);
+    if (st != KDA_OK) return st;
+    if (n_seqs < 0 || n_seqs > kMaxSeqs) return fail(KDA_ERR_INVALID_ARG, "n_seqs %d", n_seqs);
+    if (n_slots < 0) return fail(KDA_ERR_INVALID_ARG, "n_slots < 0");
+    if (n_seqs == 0) return KDA_OK;
+    KDA_REQUIRE_PTR(q, "q");
+    KDA_REQUIRE_PTR(k, "k");
+    KDA_REQUIRE_PTR(v, "v");
+    KDA_REQUIRE_PTR(alpha, "alpha");
+    KDA_REQUIRE_PTR(beta, "beta");
+    KDA_REQUIRE_PTR(pool, "pool");
+    KDA_REQUIRE_PTR(state_slot, "state_slot");
+    KDA_REQUIRE_PTR(o, "o");
+    if (n_slots == 0) return fail(KDA_ERR_INVALID_ARG, "n_slots must be > 0");
+    if ((int64_t)n_seqs * n_heads > (int64_t)INT32_MAX)
+        return fail(KDA_ERR_INVALID_ARG, "n_seqs * n_heads too large");
+    kda::DecodeLaunch p{n_seqs, n_heads, d_k, dtype, q, k, v, alpha, beta, pool, n_slots,
+                        state_slot, o, scale, nullptr};
+    st = status_ptr(&p.status);
+    if (st != KDA_OK) return st;
+    cudaError_t e = kda::launch_decode(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return KDA_OK;
+}
+
+static kda_status_t check_copy(const void* a, const void* b, int64_t n_slots, const int32_t* slots,
+                               int32_t n, int32_t H, int32_t d_k, int32_t d_v) {
+    kda_status_t st = check_dims(H, d_k, d_v, KDA_FP32);
+    if (st != KDA_OK) return st;
+    if (n < 0) return fail(KDA_ERR_INVALID_ARG, "n < 0");
+    if (n_slots < 0) return fail(KDA_ERR_INVALID_ARG, "n_slots < 0");
+    if (n == 0) return KDA_OK;
+    KDA_REQUIRE_PTR(a, "pool/src");
+    KDA_REQUIRE_PTR(b, "dst/pool");
+    KDA_REQUIRE_PTR(slots, "slots");
+    return KDA_OK;
+}
+
+kda_status_t kda_snapshot_gather(const float* pool, int64_t n_slots, const int32_t* slots,
+                                 int32_t n, int32_t n_heads, int32_t d_k, int32_t d_v,
+                                 float* dst, void* stream) {
+    kda_status_t st = check_copy(pool, dst, n_slots, slots, n, n_heads, d_k, d_v);
+    if (st != KDA_OK || n == 0) return st;
+    uint32_t* status = nullptr;
+    st = status_ptr(&status);
+    if (st != KDA_OK) return st;
+    cudaError_t e = kda::launch_gather(pool, n_slots, slots, n, (int64_t)n_heads * d_k * d_v, dst,
+                                       status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+    return KDA_OK;
+}
+
+kda_status_t kda_snapshot_restore(const float* src, float* pool, int64_t n_slots,
+                                  const int32_t* slots, int32_t n, int32_t n_heads, int32_t d_k,
+                                  int32_t d_v, void* stream) {
+    kda_status_t st = check_copy(src, pool, n_slots, slots, n, n_heads, d_k, d_v);
+    if (st != KDA_OK || n == 0) return st;
+    uint32_t* status = nullptr;
+    st = status_ptr(&status);
+    if (st != KDA_OK) return st;
+    cudaError_t e = kda::launch_restore(src, pool, n_slots, slots, n, (int64_t)n_heads * d_k * d_v,
+                                        status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "restore launch");
+    return KDA_OK;
+}
+
+kda_status_t kda_check_status(void* stream, int32_t timeout_ms, uint32_t* bits_out) {
+    if (bits_out) *bits_out = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaEvent_t ev;
+    cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+    e = cudaEventRecord(ev, s);
+    if (e != cudaSuccess) {
+        cudaEventDestroy(ev);
+        return cuda_fail(e, "cudaEventRecord");
+    }
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        e = cudaEventQuery(ev);
+        if (e == cudaSuccess) break;
+        if (e != cudaErrorNotReady) {
+            cudaEventDestroy(ev);
+            return cuda_fail(e, "stream drain");
+        }
+        if (timeout_ms > 0 &&
+            std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(timeout_ms)) {
+            cudaEventDestroy(ev);
+            return fail(KDA_ERR_TIMEOUT, "stream did not drain within %d ms", timeout_ms);
+        }
+        std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+    cudaEventDestroy(ev);
+    uint32_t bits = 0;
+    e = cudaMemcpyFromSymbol(&bits, g_status_word, sizeof bits);
+    if (e != cudaSuccess) return cuda_fail(e, "read status word");
+    if (bits) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+        if (bits_out) *bits_out = bits;
+        return fail(KDA_ERR_DEVICE_STATUS, "device status bits 0x%x", bits);
+    }
+    return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Internal helpers shared by the KDA kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Element access for the two storage types of q, k, v, o.
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float load(const float* p) { return *p; }
+    static __device__ __forceinline__ void store(float* p, float x) { *p = x; }
+    static __device__ __forceinline__ float cvt(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16* p) {
+        return __bfloat162float(*p);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16* p, float x) {
+        *p = __float2bfloat16_rn(x);
+    }
+    static __device__ __forceinline__ __nv_bfloat16 cvt(float x) { return __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ void flag(uint32_t* status, uint32_t bit) {
+    atomicOr(status, bit);
+}
+
+// Counts kernel launches (kda_launch_count); every launcher calls it once per launch.
+void note_launch(int n = 1);
+
+// ----------------------------------------------------------------- launchers
+// Each returns the cudaError_t of its launch.  Arguments were validated by the
+// C-ABI layer.
+
+struct PrefillLaunch {
+    kda_prefill_args a;
+    int32_t* order;    // workspace: sequences by decreasing chunk count
+    uint32_t* status;  // device status word
+};
+
+cudaError_t launch_prefill_token(const PrefillLaunch& p, cudaStream_t s);
+
+struct DecodeLaunch {
+    int32_t n_seqs, H, D, dtype;
+    const void *q, *k, *v;
+    const float *alpha, *beta;
+    float* pool;
+    int64_t n_slots;
+    const int32_t* slot;
+    void* o;
+    float scale;
+    uint32_t* status;
+};
+cudaError_t launch_decode(const DecodeLaunch& p, cudaStream_t s);
+
+cudaError_t launch_gather(const float* pool, int64_t n_slots, const int32_t* slots, int32_t n,
+                          int64_t slot_elems, float* dst, uint32_t* status, cudaStream_t s);
+cudaError_t launch_restore(const float* src, float* pool, int64_t n_slots, const int32_t* slots,
+                           int32_t n, int64_t slot_elems, uint32_t* status, cudaStream_t s);
+
+}  // namespace kda

@@ -110,3 +110,99 @@ def gen_states(n, H, d_k, d_v, seed, std=0.05):
     g = _stream(seed, 999_999_937)
     return (torch.randn((n, H, d_k, d_v), generator=g, dtype=torch.float64) * std).to(
         torch.float32)
+
+
+# The five workloads the layer is exercised on (sizes and seeds only).
+WORKLOADS = {
+    # tiny fp32 check: one sequence, resumed from its snapshot at t = 256
+    "tiny_fp32": dict(n_seqs=1, H=2, T=512, d=64, dtype="fp32", seed=20260, resume_at=256),
+    # prefill: 4 sequences x 8192 tokens, 32 heads, d = 128, bf16 q/k/v
+    "prefill_4x8k": dict(n_seqs=4, H=32, T=8192, d=128, dtype="bf16", seed=20261),
+    # long context: one sequence of 2^20 tokens, 8 heads, resumed at 2^19
+    "long_1m": dict(n_seqs=1, H=8, T=1 << 20, d=128, dtype="bf16", seed=20262, resume_at=1 << 19),
+    # decode: 512 sequences x 32 heads, 64 consecutive steps, states ~ N(0, 0.05^2)
+    "decode_512x32": dict(n_seqs=512, H=32, d=128, dtype="bf16", seed=20263, steps=64, state_std=0.05),
+    # mixed varlen: 64 sequences, lengths uniform in [1, 16384]; 32 of them resume
+    # inside a shared 4096-token prefix at a multiple of 256
+    "varlen_64": dict(n_seqs=64, H=32, d=128, dtype="bf16", seed=20264, max_len=16384,
+                      prefix_len=4096, n_resume=32),
+}
+
+PREFIX_STREAM = 1_000_001
+LAYOUT_STREAM = 1_000_000
+
+
+def torch_dtype(name):
+    return {"bf16": torch.bfloat16, "fp32": torch.float32}[name]
+
+
+def _draw_into(g, L, H, d_k, d_v, dtype, decay, dst, off):
+    """Draw L tokens block by block from g into the packed tensors of dst at off."""
+    for b in range(0, L, BLOCK):
+        n = min(BLOCK, L - b)
+        qb, kb, vb, ab, bb = gen_sequence_block(g, BLOCK, H, d_k, d_v, decay)
+        sl = slice(off + b, off + b + n)
+        dst["q"][sl] = qb[:n].to(dtype)
+        dst["k"][sl] = kb[:n].to(dtype)
+        dst["v"][sl] = vb[:n].to(dtype)
+        dst["alpha"][sl] = ab[:n].to(torch.float32)
+        dst["beta"][sl] = bb[:n].to(torch.float32)
+
+
+def _empty(T, H, d_k, d_v, dtype, pin=False):
+    kw = {"pin_memory": True} if pin else {}
+    return {"q": torch.empty((T, H, d_k), dtype=dtype, **kw),
+            "k": torch.empty((T, H, d_k), dtype=dtype, **kw),
+            "v": torch.empty((T, H, d_v), dtype=dtype, **kw),
+            "alpha": torch.empty((T, H, d_k), dtype=torch.float32, **kw),
+            "beta": torch.empty((T, H), dtype=torch.float32, **kw)}
+
+
+def gen_varlen_resume(n_seqs, H, d_k, d_v, max_len, prefix_len, n_resume, seed,
+                      dtype=torch.bfloat16, decay="config", interval=256, pin=False):
+    """A packed varlen batch in which some sequences resume inside a shared prefix.
+
+    Lengths L_i are uniform in [1, max_len].  ``n_resume`` sequences chosen among
+    those with L_i > interval share their first min(L_i, prefix_len) tokens with
+    one common prefix (drawn from its own stream) and resume at p_i = interval * m,
+    m uniform in [1, min(prefix_len, L_i - 1) // interval]; only their tokens
+    [p_i, L_i) are packed.  The other sequences are packed whole from position 0.
+
+    Returns dict: packed q, k, v, alpha, beta, cu_seqlens (int32), start_pos
+    (int32), lens (full lengths), resumed (sorted indices), and ``prefix`` (the
+    shared prefix's own tensors, [prefix_len, H, .]).
+    """
+    g = _stream(seed, LAYOUT_STREAM)
+    lens = torch.randint(1, max_len + 1, (n_seqs,), generator=g).tolist()
+    eligible = [i for i in range(n_seqs) if lens[i] > interval]
+    perm = torch.randperm(len(eligible), generator=g).tolist()
+    resumed = sorted(eligible[j] for j in perm[:n_resume])
+    start = [0] * n_seqs
+    for i in resumed:
+        m_max = min(prefix_len, lens[i] - 1) // interval
+        start[i] = interval * int(torch.randint(1, m_max + 1, (1,), generator=g))
+
+    prefix = _empty(prefix_len, H, d_k, d_v, dtype)
+    _draw_into(_stream(seed, PREFIX_STREAM), prefix_len, H, d_k, d_v, dtype, decay, prefix, 0)
+
+    packed_lens = [lens[i] - start[i] for i in range(n_seqs)]
+    T = sum(packed_lens)
+    out = _empty(T, H, d_k, d_v, dtype, pin)
+    off = 0
+    for i in range(n_seqs):
+        L, p = lens[i], start[i]
+        if i in resumed:
+            own = _empty(L, H, d_k, d_v, dtype)
+            _draw_into(_stream(seed, i), L, H, d_k, d_v, dtype, decay, own, 0)
+            shared = min(L, prefix_len)
+            for key in own:
+                own[key][:shared] = prefix[key][:shared]
+                out[key][off:off + L - p] = own[key][p:L]
+        else:
+            _draw_into(_stream(seed, i), L, H, d_k, d_v, dtype, decay, out, off)
+        off += L - p
+    cu = torch.zeros(n_seqs + 1, dtype=torch.int32)
+    cu[1:] = torch.tensor(np.cumsum(packed_lens), dtype=torch.int32)
+    out.update({"cu_seqlens": cu, "start_pos": torch.tensor(start, dtype=torch.int32),
+                "lens": lens, "resumed": resumed, "prefix": prefix})
+    return out

@@ -1,0 +1,201 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) KDA library, libkda.so.
+ *
+ * KDA (Kimi Delta Attention) is the linear-attention layer that makes up most of
+ * Kimi K3's layers.  Per head it keeps one fixed-size recurrent state
+ * S in R^{d_k x d_v} (fp32 here) that is updated in place for every token
+ * ("Kimi K3 Tech Intro", section 2.1; the vLLM Kimi K3 launch post, "Kimi Delta
+ * Attention" paragraph).  The update is the gated delta rule with a
+ * per-channel decay alpha_t in (0,1)^{d_k} and a write strength beta_t in (0,1):
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * The library has two modes: a chunked prefill over a packed variable-length
+ * batch that writes state snapshots every snap_interval tokens and can resume
+ * from one ("Kimi K3 Tech Intro", sections 2.2-2.4: the 256-token prefix-match
+ * unit, copy-on-write reuse of a cached state), and a batched single-token
+ * decode step that updates states in place ("Kimi K3 Tech Intro", section 4.1,
+ * the fused KDA decode kernel).  Two copy calls move states between the
+ * block-indexed state pool and contiguous buffers (copy-on-write, section 2.3).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise, owned
+ *    by the caller.  The library never allocates device memory; the only
+ *    scratch is the caller's workspace (prefill).
+ *  - Layouts are row-major with the last index contiguous:
+ *      q, k   [T, H, d_k]      v, o  [T, H, d_v]       (T = tokens, H = heads)
+ *      alpha  [T, H, d_k] fp32 beta  [T, H] fp32
+ *      state pool [n_slots, H, d_k, d_v] fp32: one slot holds the H states of
+ *      one sequence at one position.
+ *    q, k, v, o share one element type (kda_dtype_t).  Device pointers must be
+ *    16-byte aligned.
+ *  - Supported shapes: d_k == d_v in {64, 128}; chunk == 64; snap_interval == 256.
+ *    Anything else returns KDA_ERR_UNSUPPORTED.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and run on the current CUDA device.  Argument errors that
+ *    the host can see come back synchronously, before anything is launched.  A
+ *    failed launch returns KDA_ERR_CUDA.  Bad indices that only the device can
+ *    see (a slot outside the pool, a start position that is not a multiple of
+ *    snap_interval, a decreasing cu_seqlens, a snapshot ordinal beyond the
+ *    table) never trap: the kernel skips that work and sets a bit in a per-device
+ *    status word that kda_check_status() reports.
+ *  - Copy-on-write is the caller's job, as in the pages' design (section 2.3):
+ *    a state that other requests still share must be copied to a private slot
+ *    (kda_snapshot_gather / kda_snapshot_restore) before a call that writes it,
+ *    and a snapshot written by a call must not be read by another sequence of
+ *    the same call (reuse waits for the next step, section 2.4).  Decode slots
+ *    must be distinct; the library does not check this.
+ *
+ * Every function returns a kda_status_t; kda_status_string() names it and
+ * kda_last_error() gives a one-line description of the last failure on the
+ * calling host thread.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,   /* null pointer, negative count, misaligned pointer, small workspace */
+    KDA_ERR_UNSUPPORTED = 2,   /* shape or dtype outside the supported set */
+    KDA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    KDA_ERR_DEVICE_STATUS = 4, /* kda_check_status: a kernel flagged bad indices */
+    KDA_ERR_TIMEOUT = 5        /* kda_check_status: the stream did not drain in time */
+} kda_status_t;
+
+typedef enum {
+    KDA_BF16 = 0, /* q, k, v, o stored as bfloat16 */
+    KDA_FP32 = 1  /* q, k, v, o stored as float */
+} kda_dtype_t;
+
+/* Bits of the device status word (kda_device_status). */
+#define KDA_DEV_BAD_SLOT      0x1u /* init / snapshot / decode / copy slot outside [0, n_slots) */
+#define KDA_DEV_BAD_START     0x2u /* start_pos < 0 or not a multiple of snap_interval */
+#define KDA_DEV_BAD_SEQLENS   0x4u /* cu_seqlens decreasing, or past total_tokens */
+#define KDA_DEV_BAD_ORDINAL   0x8u /* snapshot ordinal >= snap_table_stride */
+
+/*
+ * Chunked prefill over a packed variable-length batch.
+ *
+ * Sequence s owns tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 of the packed
+ * tensors.  Its first token sits at absolute position start_pos[s] (0 when
+ * start_pos is NULL), which must be a multiple of snap_interval: a resume starts
+ * at a snapshot boundary ("Kimi K3 Tech Intro", section 2.4: the scheduler stops
+ * at a hash boundary).  Its initial states are pool slot init_slot[s] (all H
+ * heads), or zero when init_slot is NULL or init_slot[s] == -1.
+ *
+ * After the token that ends at absolute position p, for every p that is a
+ * positive multiple of snap_interval, the H states are written to pool slot
+ * snap_table[s * snap_table_stride + p / snap_interval - 1] unless that entry is
+ * -1 (snapshot ordinals are absolute, so a resumed sequence continues the
+ * numbering of the run it resumes).  snap_table may be NULL (no snapshots).
+ * The states after each sequence's last token go to final_state
+ * [n_seqs, H, d_k, d_v] fp32 unless it is NULL.  Outputs go to o.
+ *
+ * Chunks are aligned to absolute multiples of `chunk`, and every reduction has
+ * a fixed order, so a resumed run reproduces a full run bit for bit.
+ */
+typedef struct kda_prefill_args {
+    int32_t n_seqs;            /* >= 0 */
+    int32_t n_heads;           /* H >= 1 */
+    int32_t d_k;               /* 64 or 128 */
+    int32_t d_v;               /* == d_k */
+    int32_t chunk;             /* 64 */
+    int32_t snap_interval;     /* 256 */
+    int32_t dtype;             /* kda_dtype_t of q, k, v, o */
+    float scale;               /* output scale (1 for the plain rule) */
+    int64_t total_tokens;      /* host copy of cu_seqlens[n_seqs] */
+    int64_t n_slots;           /* slots in pool (0 if pool is NULL) */
+    int32_t snap_table_stride; /* entries per sequence in snap_table */
+    int32_t reserved0;         /* must be 0 */
+    const void *q, *k, *v;     /* [T, H, d_k], [T, H, d_k], [T, H, d_v] */
+    const float *alpha;        /* [T, H, d_k], each in (0, 1] */
+    const float *beta;         /* [T, H] */
+    const int32_t *cu_seqlens; /* [n_seqs + 1], cu_seqlens[0] = 0, non-decreasing */
+    const int32_t *start_pos;  /* [n_seqs] or NULL */
+    const int32_t *init_slot;  /* [n_seqs] or NULL */
+    float *pool;               /* [n_slots, H, d_k, d_v] or NULL */
+    const int32_t *snap_table; /* [n_seqs, snap_table_stride] or NULL */
+    void *o;                   /* [T, H, d_v] */
+    float *final_state;        /* [n_seqs, H, d_k, d_v] or NULL */
+    void *workspace;           /* >= kda_prefill_workspace_size(args) bytes, 256-B aligned */
+    size_t workspace_bytes;
+} kda_prefill_args;
+
+/* Bytes of workspace kda_prefill_chunked needs for these arguments (only the
+ * sizes are read).  Returns 0 when the sizes are invalid. */
+size_t kda_prefill_workspace_size(const kda_prefill_args *args);
+
+/* Chunked prefill; see kda_prefill_args.  `args` is a host pointer, read
+ * before the call returns. */
+kda_status_t kda_prefill_chunked(const kda_prefill_args *args, void *stream);
+
+/*
+ * One decode step for n_seqs sequences, one token each ("Kimi K3 Tech Intro",
+ * section 4.1: the recurrent update of the fused decode kernel, with the state
+ * updated in place).  Sequence s reads and rewrites the H states in pool slot
+ * state_slot[s]:
+ *     S <- (I - beta k k^T) Diag(alpha) S + beta k v^T ;  o = scale * S^T q
+ * q, k [n_seqs, H, d_k]; v, o [n_seqs, H, d_v]; alpha [n_seqs, H, d_k];
+ * beta [n_seqs, H]; state_slot [n_seqs] device int32.  Slots must be distinct.
+ */
+kda_status_t kda_decode_step(int32_t n_seqs, int32_t n_heads, int32_t d_k, int32_t d_v,
+                             int32_t dtype, const void *q, const void *k, const void *v,
+                             const float *alpha, const float *beta, float *pool,
+                             int64_t n_slots, const int32_t *state_slot, void *o,
+                             float scale, void *stream);
+
+/*
+ * Copy n pool slots out to a contiguous buffer: dst[i] = pool[slots[i]]
+ * (H x d_k x d_v fp32 each; slots[i] == -1 writes zeros).  The private copy of
+ * copy-on-write reuse ("Kimi K3 Tech Intro", section 2.3); bit-exact.
+ */
+kda_status_t kda_snapshot_gather(const float *pool, int64_t n_slots, const int32_t *slots,
+                                 int32_t n, int32_t n_heads, int32_t d_k, int32_t d_v,
+                                 float *dst, void *stream);
+
+/*
+ * Copy n contiguous states into pool slots: pool[slots[i]] = src[i]
+ * (slots[i] == -1 skips entry i).  Target slots must be distinct; bit-exact.
+ */
+kda_status_t kda_snapshot_restore(const float *src, float *pool, int64_t n_slots,
+                                  const int32_t *slots, int32_t n, int32_t n_heads,
+                                  int32_t d_k, int32_t d_v, void *stream);
+
+/*
+ * Wait for `stream` to drain (at most timeout_ms milliseconds; <= 0 waits
+ * without limit), then read and clear the current device's status word.
+ * Returns KDA_OK, KDA_ERR_DEVICE_STATUS (bits in *bits_out when non-NULL),
+ * KDA_ERR_TIMEOUT (the word is left untouched) or KDA_ERR_CUDA.  Calls on
+ * several streams of one device share the word.
+ */
+kda_status_t kda_check_status(void *stream, int32_t timeout_ms, uint32_t *bits_out);
+
+/* Name of a status code (static string). */
+const char *kda_status_string(kda_status_t status);
+
+/* One-line description of the last failure on this host thread (static storage). */
+const char *kda_last_error(void);
+
+/* KDA_ABI_VERSION of the loaded library. */
+int32_t kda_abi_version(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all host threads).  A diagnostic for counting launches in a timed region. */
+uint64_t kda_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */
