@@ -8,7 +8,7 @@
 #include <mutex>
 #include <thread>
 
-#include "kda_common.cuh"
+#include "chunk_common.cuh"
 
 namespace {
 
@@ -111,11 +111,34 @@ kda_status_t validate_prefill(const kda_prefill_args* a) {
 
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
-// Workspace of the path the arguments select (bytes, 256-byte multiple).
-size_t workspace_bytes_for(const kda_prefill_args* a) {
-    (void)a;
-    return 0;
+bool use_chunked(const kda_prefill_args* a) { return a->dtype == KDA_BF16 && a->d_k == 128; }
+
+// Upper bound on the chunks of a batch: each sequence starts chunk-aligned
+// (start_pos is a multiple of snap_interval), so it has at most one partial chunk.
+int64_t max_chunks_for(const kda_prefill_args* a) {
+    return a->total_tokens / kda::kC + a->n_seqs;
 }
+
+struct WorkspaceLayout {
+    size_t chunk_base, chain_flag, records, total;
+};
+
+WorkspaceLayout layout_for(const kda_prefill_args* a) {
+    WorkspaceLayout w{};
+    if (!use_chunked(a) || a->n_seqs == 0) return w;
+    size_t off = 0;
+    w.chunk_base = off;
+    off = round_up(off + sizeof(int32_t) * ((size_t)a->n_seqs + 1), 256);
+    w.chain_flag = off;
+    off = round_up(off + sizeof(int32_t) * (size_t)a->n_seqs * a->n_heads, 256);
+    w.records = off;
+    off += (size_t)max_chunks_for(a) * a->n_heads * kda::kRecBytes;
+    w.total = round_up(off, 256);
+    return w;
+}
+
+// Workspace of the path the arguments select (bytes, 256-byte multiple).
+size_t workspace_bytes_for(const kda_prefill_args* a) { return layout_for(a).total; }
 
 std::atomic<uint64_t> g_launches{0};
 
@@ -157,14 +180,38 @@ kda_status_t kda_prefill_chunked(const kda_prefill_args* a, void* stream) {
     if (need > 0 && (!a->workspace || a->workspace_bytes < need ||
                      (reinterpret_cast<uintptr_t>(a->workspace) & 255u)))
         return fail(KDA_ERR_INVALID_ARG, "workspace must be >= %zu bytes and 256-byte aligned", need);
-    kda::PrefillLaunch p;
-    p.a = *a;
-    p.order = nullptr;
-    st = status_ptr(&p.status);
+    uint32_t* status = nullptr;
+    st = status_ptr(&status);
     if (st != KDA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = kda::launch_prefill_token(p, s);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    kda::PrefillLaunch p;
+    p.a = *a;
+    p.chain_flag = nullptr;
+    p.status = status;
+    if (!use_chunked(a)) {
+        cudaError_t e = kda::launch_prefill_token(p, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+        return KDA_OK;
+    }
+    const WorkspaceLayout w = layout_for(a);
+    uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+    kda::ChunkLaunch c;
+    c.a = *a;
+    c.chunk_base = reinterpret_cast<int32_t*>(ws + w.chunk_base);
+    c.chain_flag = reinterpret_cast<int32_t*>(ws + w.chain_flag);
+    c.records = ws + w.records;
+    c.max_chunks = max_chunks_for(a);
+    c.status = status;
+    cudaError_t e = kda::launch_chunk_meta(c, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill meta launch");
+    e = kda::launch_chunk_local(c, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill chunk-local launch");
+    e = kda::launch_chunk_recur(c, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill chunk-recurrence launch");
+    // chains whose gates left the factorisation's range: token by token
+    p.chain_flag = c.chain_flag;
+    e = kda::launch_prefill_token(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill fallback launch");
     return KDA_OK;
 }
 

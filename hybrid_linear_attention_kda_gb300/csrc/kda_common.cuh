@@ -39,8 +39,8 @@ void note_launch(int n = 1);
 
 struct PrefillLaunch {
     kda_prefill_args a;
-    int32_t* order;    // workspace: sequences by decreasing chunk count
-    uint32_t* status;  // device status word
+    const int32_t* chain_flag;  // [n_seqs * H] or NULL: when set, only flagged (seq, head) run
+    uint32_t* status;           // device status word
 };
 
 cudaError_t launch_prefill_token(const PrefillLaunch& p, cudaStream_t s);

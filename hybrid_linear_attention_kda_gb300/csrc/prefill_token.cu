@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(NT) prefill_token_kernel(PrefillLaunch p) {
     const int seq = (int)(sh / H);
     const int head = (int)(sh - (int64_t)seq * H);
     const int j0 = tile * TJ;
+    if (p.chain_flag && !p.chain_flag[sh]) return;
 
     const int64_t t_begin = a.cu_seqlens[seq], t_end = a.cu_seqlens[seq + 1];
     if (t_end < t_begin || t_end > a.total_tokens || t_begin < 0) {

@@ -1,0 +1,208 @@
+// Blackwell (sm_100 family) building blocks written as inline PTX: tensor memory
+// (TMEM) allocation, tcgen05 MMAs with shared-memory operand descriptors, TMEM
+// loads, mbarriers with bounded waits, and bulk (TMA engine) copies.
+//
+// Operand layouts.  Every MMA operand here is bf16 in shared memory in the
+// 128-byte swizzled canonical layout: "atoms" of 8 rows x 128 bytes (1024 B,
+// 1024-byte aligned) in which the 16-byte chunk j of row r is stored at chunk
+// position j ^ (r % 8).
+//   K-major  [R rows x K] (K contiguous, K a multiple of 64): the K range is cut
+//            into 64-wide column regions of R x 128 B each; inside a region the
+//            8-row atoms follow each other (stride-byte-offset = 1024).  An MMA
+//            k-step of 16 elements starts 32 bytes further inside the region.
+//   MN-major [K rows x MN] (MN contiguous, MN a multiple of 64): atoms of 8 K
+//            rows x 64 MN elements; consecutive 64-wide MN blocks are
+//            leading-byte-offset apart and consecutive 8-row K groups are
+//            stride-byte-offset apart.  A k-step of 16 spans two K groups.
+// For a 64-wide contiguous dimension both layouts are the same bytes: a
+// [rows x 64] tile can serve as K-major (K = the 64) or MN-major (MN = the 64).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace kda {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------------ layouts
+
+// Byte offset of element (row, k) in a K-major SW128 bf16 tile of R rows.
+__host__ __device__ __forceinline__ uint32_t kmajor_off(uint32_t row, uint32_t k, uint32_t R) {
+    return (k >> 6) * (R * 128u) + (row >> 3) * 1024u + (row & 7u) * 128u +
+           ((((k & 63u) >> 3) ^ (row & 7u)) << 4) + (k & 7u) * 2u;
+}
+
+// Byte offset of the 16-byte chunk holding elements (row, 8c .. 8c+7) of a
+// [rows x 64] SW128 tile (either major-ness).
+__host__ __device__ __forceinline__ uint32_t row64_chunk_off(uint32_t row, uint32_t c) {
+    return (row >> 3) * 1024u + (row & 7u) * 128u + ((c ^ (row & 7u)) << 4);
+}
+
+// Byte offset of element (mn, k) in an MN-major SW128 bf16 tile with the given
+// leading (MN block) and stride (K group) byte offsets.
+__host__ __device__ __forceinline__ uint32_t mnmajor_off(uint32_t mn, uint32_t k, uint32_t lbo,
+                                                         uint32_t sbo) {
+    return (k >> 3) * sbo + (mn >> 6) * lbo + (k & 7u) * 128u +
+           ((((mn & 63u) >> 3) ^ (k & 7u)) << 4) + (mn & 7u) * 2u;
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and stride
+// byte offsets (all >> 4), descriptor version 1 (bit 46), swizzle mode 2 =
+// 128-byte swizzle (bits 61-63).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator.
+// a_mn / b_mn select MN-major operands; N in [8, 256] step 8 (16 for M = 128).
+__host__ __device__ __forceinline__ uint32_t idesc_bf16(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
+    return (1u << 4)                       // D format: f32
+         | (1u << 7)                       // A format: bf16
+         | (1u << 10)                      // B format: bf16
+         | ((a_mn ? 1u : 0u) << 15)
+         | ((b_mn ? 1u : 0u) << 16)
+         | ((N >> 3) << 17)
+         | ((M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ fences
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ mbarriers
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase with the given parity to complete; false after
+// `limit` clock cycles (about a second at the default) without completion.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          long long limit = 2000000000LL) {
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity)) {
+        if (clock64() - t0 > limit) return false;
+    }
+    return true;
+}
+
+// ------------------------------------------------------------------ bulk copies
+
+// global -> shared, completion counted (bytes) on `bar`.  16-byte aligned, size % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// shared -> global in the current bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until the shared-memory sources of all committed groups have been read
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// wait until all committed groups have completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// ------------------------------------------------------------------ TMEM
+
+// Allocate ncols TMEM columns (power of two >= 32); executed by one whole warp.
+// The base address is written to *slot (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[smem desc] x B[smem desc]^T, kind::f16, one CTA.  Issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns: thread i of the warp reads lane
+// (taddr.lane + i).  The warp's lane quarter must be (warp id % 4).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ packing
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+}  // namespace tc
+}  // namespace kda

@@ -32,7 +32,9 @@
  *    q, k, v, o share one element type (kda_dtype_t).  Device pointers must be
  *    16-byte aligned.
  *  - Supported shapes: d_k == d_v in {64, 128}; chunk == 64; snap_interval == 256.
- *    Anything else returns KDA_ERR_UNSUPPORTED.
+ *    Anything else returns KDA_ERR_UNSUPPORTED.  bf16 inputs with d = 128 take
+ *    the chunked tensor-core path; fp32 inputs and d = 64 are evaluated token by
+ *    token with the fp32 state in registers (same results within rounding).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream) and run on the current CUDA device.  Argument errors that
  *    the host can see come back synchronously, before anything is launched.  A
@@ -83,6 +85,7 @@ typedef enum {
 #define KDA_DEV_BAD_START     0x2u /* start_pos < 0 or not a multiple of snap_interval */
 #define KDA_DEV_BAD_SEQLENS   0x4u /* cu_seqlens decreasing, or past total_tokens */
 #define KDA_DEV_BAD_ORDINAL   0x8u /* snapshot ordinal >= snap_table_stride */
+#define KDA_DEV_WAIT_TIMEOUT  0x10u /* a kernel gave up waiting on its own copies / MMAs (about 1 s) */
 
 /*
  * Chunked prefill over a packed variable-length batch.
