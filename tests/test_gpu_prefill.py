@@ -207,10 +207,9 @@ def test_bad_start_position_is_reported_and_skipped(kda, cuda_device):
     data = inputs.gen_prefill([100, 100], 2, 128, 128, 81)
     o = torch.full((200, 2, 128), 7.0, dtype=torch.bfloat16, device=dev)
     x = to_dev(data, dev)
-    args = kda.make_prefill_args(x["q"], x["k"], x["v"], x["alpha"], x["beta"],
-                                 data["cu_seqlens"].to(dev), 200, o,
-                                 start_pos=torch.tensor([0, 100], dtype=torch.int32, device=dev))
-    kda.kda_prefill_chunked(args)
+    kda.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], data["cu_seqlens"].to(dev),
+                total_tokens=200, start_pos=torch.tensor([0, 100], dtype=torch.int32, device=dev),
+                o=o)
     assert kda.kda_check_status() & kda.KDA_DEV_BAD_START
     assert torch.all(o[100:] == 7.0)                      # the bad sequence wrote nothing
     assert not torch.all(o[:100] == 7.0)
