@@ -16,7 +16,7 @@
 //                                    cols 160..191 k_r rho_r   -> A, r in half 1, s in half 0
 // Within a half the factors phi, psi span at most 16 tokens; a chunk whose
 // factors leave [2^-100, 2^100] flags its (sequence, head) for the token-serial
-// kernel.  T = (I + A)^-1 is solved column by column in fp32, then W and U~ come
+// kernel.  T = (I + A)^-1 is inverted by 16 x 16 blocks in fp32, then W and U~ come
 // from a second MMA (X^T T^T and Y^T T^T with X = diag(beta) Gamma K,
 // Y = diag(beta) V).
 #include "chunk_common.cuh"
@@ -34,6 +34,8 @@ constexpr uint32_t kAmat = 0;           // after the A/P MMA: A fp32 [64][64]
 constexpr uint32_t kTm = 16384;         //   T as MN-major [s][r] bf16
 constexpr uint32_t kXt = 24576;         //   X^T K-major [c][s]
 constexpr uint32_t kYt = 40960;         //   Y^T K-major [j][s]
+constexpr uint32_t kTf = 57344;         //   T fp32 [64][64]
+constexpr uint32_t kTscr = 73728;       //   block-product scratch, 3 x 16 x 16 fp32
 constexpr uint32_t kMisc = 81920;
 constexpr size_t kSmemBytes = kMisc + 2048 + 1024;
 
@@ -59,6 +61,56 @@ __device__ __forceinline__ void stg16(uint8_t* p, uint4 v) { *reinterpret_cast<u
 // byte offset of the 16-byte chunk (mn .. mn+7, k) in an MN-major tile
 __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k, uint32_t lbo, uint32_t sbo) {
     return (k >> 3) * sbo + (mn >> 6) * lbo + (k & 7u) * 128u + ((((mn & 63u) >> 3) ^ (k & 7u)) << 4);
+}
+
+
+// T = (I + A)^-1 for a strictly lower triangular 64 x 64 A (fp32, row-major),
+// by 16 x 16 blocks: the four diagonal blocks by forward substitution, then the
+// off-diagonal blocks one block-diagonal at a time,
+//     T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj .
+// All 256 threads take part; T (including zeros above the diagonal inside the
+// diagonal blocks) goes to Tf, row-major.  Ends with a barrier.
+__device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, float* scr, int tid) {
+    if (tid < kC) {
+        const int o = 16 * (tid >> 4), jj = tid & 15;
+        float t[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = r == jj ? 1.f : 0.f;
+#pragma unroll
+            for (int u = 0; u < r; ++u) acc = fmaf(-A[(o + r) * kC + o + u], t[u], acc);
+            t[r] = acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Tf[(o + r) * kC + o + jj] = t[r];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int dist = 1; dist < 4; ++dist) {
+        const int nblk = 4 - dist;
+        for (int e = tid; e < nblk * 256; e += kThreads) {       // M = sum_k A_ik T_kj
+            const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+            const int i = dist + blk, jb = i - dist;
+            float acc = 0.f;
+            for (int kb = jb; kb < i; ++kb) {
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    acc = fmaf(A[(16 * i + rr) * kC + 16 * kb + u], Tf[(16 * kb + u) * kC + 16 * jb + cc], acc);
+            }
+            scr[e] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < nblk * 256; e += kThreads) {       // T_ij = -T_ii M
+            const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+            const int i = dist + blk, jb = i - dist;
+            float acc = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                acc = fmaf(Tf[(16 * i + rr) * kC + 16 * i + u], scr[(blk << 8) + (u << 4) + cc], acc);
+            Tf[(16 * i + rr) * kC + 16 * jb + cc] = -acc;
+        }
+        __syncthreads();
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 2) chunk_local_kernel(ChunkLaunch p) {
@@ -135,9 +187,11 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_local_kernel(ChunkLaunch p)
 
     bool guard_bad = false;
     const uint32_t apa = s_base + kAPa, apb = s_base + kAPb;
-    {   // forward walk: Gamma (Q~), rho (half 1), phi/psi for local tokens 16..31
-        float P = 1.f, E = 1.f;
-        float gq[8], oq[8], ok[8], dq[8], dk[8], dd[8];
+    // Each walk below keeps one running product; splitting the walks keeps only
+    // a few 8-token staging groups live at a time.
+    {   // forward: Gamma (Q~ to the record), rho (half 1: q rho, k rho)
+        float P = 1.f;
+        float gq[8], oq[8], ok[8];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
@@ -146,14 +200,6 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_local_kernel(ChunkLaunch p)
             gq[i & 7] = qf * (hh ? H0 * P : P);
             oq[i & 7] = qf * P;
             ok[i & 7] = kf * P;
-            if (i >= 16) {
-                E *= al[i];
-                guard_bad |= !(E >= kGuardMin);
-                const float inv = 1.f / E;
-                dq[i & 7] = qf * E;
-                dk[i & 7] = kf * E;
-                dd[i & 7] = kf * inv;
-            }
             if ((i & 7) == 7) {
                 const uint32_t r0 = 32 * hh + (i & ~7);
                 stg16(rec + kRecQ + row64_chunk_off(c, r0 >> 3), pack8(gq));
@@ -161,43 +207,66 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_local_kernel(ChunkLaunch p)
                     sts16(apb + mn_chunk(64 + (i & ~7), c, kLboB, kSboB), pack8(oq));
                     sts16(apb + mn_chunk(160 + (i & ~7), c, kLboB, kSboB), pack8(ok));
                 }
-                if (i >= 16) {
-                    sts16(apb + mn_chunk(r0, c, kLboB, kSboB), pack8(dq));
-                    sts16(apb + mn_chunk(96 + r0, c, kLboB, kSboB), pack8(dk));
-                    sts16(apa + mn_chunk(r0, c, kLboA, kSboA), pack8(dd));
-                }
             }
         }
     }
-    {   // backward walk: kappa (Kbar), sigma (half 0), phi/psi for local tokens 0..15
-        float Q = 1.f, Dd = 1.f;
-        float kb[8], kc[8], dq[8], dk[8], dd[8];
+    {   // forward from the half's reference token: phi = E, psi = 1/E (local tokens 16..31)
+        float E = 1.f;
+        float dq[8], dk[8], dd[8];
+#pragma unroll
+        for (int i = 16; i < 32; ++i) {
+            const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
+            const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+            E *= al[i];
+            guard_bad |= !(E >= kGuardMin);
+            const float inv = __fdividef(1.f, E);
+            dq[i & 7] = qf * E;
+            dk[i & 7] = kf * E;
+            dd[i & 7] = kf * inv;
+            if ((i & 7) == 7) {
+                const uint32_t r0 = 32 * hh + (i & ~7);
+                sts16(apb + mn_chunk(r0, c, kLboB, kSboB), pack8(dq));
+                sts16(apb + mn_chunk(96 + r0, c, kLboB, kSboB), pack8(dk));
+                sts16(apa + mn_chunk(r0, c, kLboA, kSboA), pack8(dd));
+            }
+        }
+    }
+    {   // backward: kappa (Kbar to the record), sigma (half 0: k sigma); zero pad rows
+        float Q = 1.f;
+        float kb[8], kc[8];
 #pragma unroll
         for (int i = 31; i >= 0; --i) {
-            const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
             const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
             kb[i & 7] = kf * (hh ? Q : Q * H1);
             kc[i & 7] = kf * Q;
-            if (i <= 15) {
-                guard_bad |= !(Dd >= kGuardMin);
-                const float inv = 1.f / Dd;
-                dq[i & 7] = qf * inv;
-                dk[i & 7] = kf * inv;
-                dd[i & 7] = kf * Dd;
-            }
             if ((i & 7) == 0) {
                 const uint32_t r0 = 32 * hh + i;
                 stg16(rec + kRecK + row64_chunk_off(c, r0 >> 3), pack8(kb));
                 if (!hh) sts16(apa + mn_chunk(64 + i, c, kLboA, kSboA), pack8(kc));
                 else sts16(apa + mn_chunk(96 + i, c, kLboA, kSboA), make_uint4(0u, 0u, 0u, 0u));
-                if (i <= 15) {
-                    sts16(apb + mn_chunk(r0, c, kLboB, kSboB), pack8(dq));
-                    sts16(apb + mn_chunk(96 + r0, c, kLboB, kSboB), pack8(dk));
-                    sts16(apa + mn_chunk(r0, c, kLboA, kSboA), pack8(dd));
-                }
             }
             Q *= al[i];
-            if (i <= 15) Dd *= al[i];
+        }
+    }
+    {   // backward to the half's reference token: phi = 1/D, psi = D (local tokens 0..15)
+        float Dd = 1.f;
+        float dq[8], dk[8], dd[8];
+#pragma unroll
+        for (int i = 15; i >= 0; --i) {
+            const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
+            const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+            guard_bad |= !(Dd >= kGuardMin);
+            const float inv = __fdividef(1.f, Dd);
+            dq[i & 7] = qf * inv;
+            dk[i & 7] = kf * inv;
+            dd[i & 7] = kf * Dd;
+            if ((i & 7) == 0) {
+                const uint32_t r0 = 32 * hh + i;
+                sts16(apb + mn_chunk(r0, c, kLboB, kSboB), pack8(dq));
+                sts16(apb + mn_chunk(96 + r0, c, kLboB, kSboB), pack8(dk));
+                sts16(apa + mn_chunk(r0, c, kLboA, kSboA), pack8(dd));
+            }
+            Dd *= al[i];
         }
     }
     if (guard_bad) atomicOr(&ms.guard_fail, 1);
@@ -279,68 +348,63 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_local_kernel(ChunkLaunch p)
     __syncthreads();
     fence_after_sync();
 
-    // ---------------------------------------------------------------- phase 3: T, X^T, Y^T
-    if (warp < 2) {
-        // column j of T = (I + A)^-1 by forward substitution, fp32
-        const int j = tid;
-        const float* Am = reinterpret_cast<const float*>(sm + kAmat);
-        float Tc[kC];
+    // ---------------------------------------------------------------- phase 3: X^T, Y^T, T
+    // X^T / Y^T rows from this thread's 32 tokens of channel c (two rounds of 16
+    // tokens, to bound the loads in flight per thread), then T.
+    {
+        float Gm = hh ? ms.tot[0][c] : 1.f;
+#pragma unroll 1
+        for (int rnd = 0; rnd < 2; ++rnd) {
+            float ax[16];
+            uint32_t kq[8], vq[8];
 #pragma unroll
-        for (int r = 0; r < kC; ++r) Tc[r] = (r == j) ? 1.f : 0.f;
-#pragma unroll
-        for (int r = 1; r < kC; ++r) {
-            float acc = 0.f;
-#pragma unroll
-            for (int s4 = 0; s4 < r; s4 += 4) {
-                const float4 a4 = *reinterpret_cast<const float4*>(Am + r * kC + s4);
-                acc = fmaf(a4.x, Tc[s4], acc);
-                acc = fmaf(a4.y, Tc[s4 + 1], acc);
-                acc = fmaf(a4.z, Tc[s4 + 2], acc);
-                acc = fmaf(a4.w, Tc[s4 + 3], acc);
+            for (int i = 0; i < 16; i += 2) {
+                const int r = 32 * hh + 16 * rnd + i;
+                const int64_t e0 = ebase + (int64_t)r * tstride + c, e1 = e0 + tstride;
+                const bool v0 = r < n, v1 = r + 1 < n;
+                ax[i] = v0 ? a.alpha[e0] : 1.f;
+                ax[i + 1] = v1 ? a.alpha[e1] : 1.f;
+                kq[i >> 1] = (v0 ? (uint32_t)__bfloat16_as_ushort(kg[e0]) : 0u) |
+                             ((v1 ? (uint32_t)__bfloat16_as_ushort(kg[e1]) : 0u) << 16);
+                vq[i >> 1] = (v0 ? (uint32_t)__bfloat16_as_ushort(vg[e0]) : 0u) |
+                             ((v1 ? (uint32_t)__bfloat16_as_ushort(vg[e1]) : 0u) << 16);
             }
-            Tc[r] = (r == j) ? 1.f : -acc;
+            // X^T row c: beta_r Gamma_rc k_rc ;  Y^T row c: beta_r v_rc
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                float x[8], y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = 8 * c2 + e;
+                    const float b = ms.beta[32 * hh + 16 * rnd + i];
+                    Gm *= ax[i];
+                    const float kf = (i & 1) ? bf_hi(kq[i >> 1]) : bf_lo(kq[i >> 1]);
+                    const float vf = (i & 1) ? bf_hi(vq[i >> 1]) : bf_lo(vq[i >> 1]);
+                    x[e] = b * kf * Gm;
+                    y[e] = b * vf;
+                }
+                const int cc = 4 * hh + 2 * rnd + c2;
+                sts16(s_base + kXt + row64_chunk_off(c, cc), pack8(x));
+                sts16(s_base + kYt + row64_chunk_off(c, cc), pack8(y));
+            }
         }
-        // T^T row j (= column j of T) as the MN-major [s][r] operand
+    }
+    invert_unit_lower(reinterpret_cast<const float*>(sm + kAmat), reinterpret_cast<float*>(sm + kTf),
+                      reinterpret_cast<float*>(sm + kTscr), tid);
+    {
+        // T^T row s (= column s of T, zero above the diagonal) as the MN-major [s][r] operand
+        const float* Tf = reinterpret_cast<const float*>(sm + kTf);
+        const int srow = tid >> 2;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = Tc[8 * cc + e];
-            sts16(s_base + kTm + row64_chunk_off(j, cc), pack8(x));
-        }
-    } else if (warp >= 4) {
-        // X^T row c: beta_r Gamma_rc k_rc
-        const int cx = tid - 128;
-        float Gm = 1.f;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
+        for (int q2 = 0; q2 < 2; ++q2) {
+            const int cc = 2 * (tid & 3) + q2;
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int r = 8 * cc + e;
-                const int64_t el = ebase + (int64_t)r * tstride + cx;
-                const bool v = r < n;
-                Gm *= v ? a.alpha[el] : 1.f;
-                x[e] = v ? ms.beta[r] * __bfloat162float(kg[el]) * Gm : 0.f;
+                x[e] = r >= srow ? Tf[r * kC + srow] : 0.f;
             }
-            sts16(s_base + kXt + row64_chunk_off(cx, cc), pack8(x));
-        }
-    } else {
-        // Y^T rows j0 and j0 + 64: beta_r v_rj
-        const int j0 = tid - 64;
-#pragma unroll
-        for (int rep = 0; rep < 2; ++rep) {
-            const int j = j0 + 64 * rep;
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int r = 8 * cc + e;
-                    x[e] = r < n ? ms.beta[r] * __bfloat162float(vg[ebase + (int64_t)r * tstride + j]) : 0.f;
-                }
-                sts16(s_base + kYt + row64_chunk_off(j, cc), pack8(x));
-            }
+            sts16(s_base + kTm + row64_chunk_off(srow, cc), pack8(x));
         }
     }
     fence_async_smem();

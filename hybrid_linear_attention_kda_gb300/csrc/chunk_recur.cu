@@ -7,10 +7,11 @@
 //   (b) D2 = S^T Q~^T
 //   (c) D2 += U^T P^T            O^T = D2
 //   (d) D3 = U^T Kbar            S^T <- S^T Diag(gamma) + D3  (fp32, registers)
-// Thread (j, half) keeps 64 fp32 state entries S[c][j] for its half of the key
-// channels c; the bf16 copy of S^T in shared memory is the A operand of (a) and
+// Thread (j, quarter) keeps 32 fp32 state entries S[c][j] for its quarter of the
+// key channels c; the bf16 copy of S^T in shared memory is the A operand of (a) and
 // (b).  The chunk records written by stage one arrive with bulk copies, two
-// chunks in flight.  A snapshot is written after every chunk that ends at an
+// chunks in flight.  The output accumulator is double-buffered so that the
+// outputs of one chunk are stored while the next chunk's MMAs run.  A snapshot is written after every chunk that ends at an
 // absolute position that is a multiple of snap_interval ("Kimi K3 Tech Intro",
 // sections 2.2-2.4), straight from the fp32 registers.
 #include "chunk_common.cuh"
@@ -19,7 +20,7 @@ namespace kda {
 namespace {
 using namespace tc;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;      // 16 warps: 4 lane quarters x 4 key-channel quarters
 constexpr uint32_t kSa = 0;               // S^T bf16, K-major [j][c], two 64-wide regions
 constexpr uint32_t kUa = 32768;           // U^T bf16, K-major [j][t]
 constexpr uint32_t kStage0 = 49152;
@@ -27,9 +28,12 @@ constexpr uint32_t kStageStride = 74752;  // kRecBytes rounded up to 1024
 constexpr uint32_t kMisc = kStage0 + 2 * kStageStride;
 constexpr size_t kSmemBytes = kMisc + 64 + 1024;
 
+constexpr uint32_t kTmemCols = 512;       // D1 [0,64), D2 x2 [64,192), D3 [256,384)
+
 struct Misc {
     uint64_t bar_load[2];
-    uint64_t bar_mma;
+    uint64_t bar_a;
+    uint64_t bar_cd;
     uint32_t tslot;
 };
 
@@ -57,23 +61,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
 
     const int jq = warp & 3, ch = warp >> 2;
     const int j = 32 * jq + lane;          // value channel (TMEM lane)
-    const int cbase = 64 * ch;             // this thread's key channels
+    const int cbase = 32 * ch;             // this thread's 32 key channels
+    const int tq = 16 * ch;                // and its 16 tokens in the per-token epilogues
     const uint32_t lanebase = (uint32_t)(32 * jq) << 16;
     const int64_t slot_stride = (int64_t)H * kD * kD;
     const int64_t head_off = (int64_t)h * kD * kD;
 
-    float S[64];
+    float S[32];
     if (init >= 0) {
         const float* S0 = a.pool + (int64_t)init * slot_stride + head_off;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) S[i] = S0[(int64_t)(cbase + i) * kD + j];
+        for (int i = 0; i < 32; ++i) S[i] = S0[(int64_t)(cbase + i) * kD + j];
     } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) S[i] = 0.f;
+        for (int i = 0; i < 32; ++i) S[i] = 0.f;
     }
     auto write_sa = [&]() {
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
+        for (int m = 0; m < 4; ++m) {
             const uint4 v = make_uint4(pack_bf16(S[8 * m], S[8 * m + 1]), pack_bf16(S[8 * m + 2], S[8 * m + 3]),
                                        pack_bf16(S[8 * m + 4], S[8 * m + 5]), pack_bf16(S[8 * m + 6], S[8 * m + 7]));
             sts16(s_base + kSa + kmajor_off(j, cbase + 8 * m, kD), v);
@@ -81,11 +86,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     };
     write_sa();
 
-    if (warp == 0) tmem_alloc(&ms.tslot, 256);
+    if (warp == 0) tmem_alloc(&ms.tslot, kTmemCols);
     if (tid == 0) {
         mbar_init(&ms.bar_load[0], 1);
         mbar_init(&ms.bar_load[1], 1);
-        mbar_init(&ms.bar_mma, 1);
+        mbar_init(&ms.bar_a, 1);
+        mbar_init(&ms.bar_cd, 1);
         fence_mbar_init();
     }
     fence_async_smem();
@@ -93,69 +99,104 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = ms.tslot;
-    const uint32_t tD1 = tbase, tD2 = tbase + 64, tD3 = tbase + 128;
+    const uint32_t tD1 = tbase, tD3 = tbase + 256;
+    auto tD2 = [&](int64_t lc) -> uint32_t { return tbase + 64 + 64 * (uint32_t)(lc & 1); };
 
+    // Thread 0 issues every copy and MMA and keeps the counts needed to drain
+    // them if a wait ever times out.
+    uint32_t ld_issued[2] = {0, 0}, ld_waited[2] = {0, 0};
+    uint32_t a_issued = 0, a_waited = 0, cd_issued = 0, cd_waited = 0;
     auto rec_ptr = [&](int64_t lc) -> const uint8_t* {
         return p.records + ((size_t)(g0 + lc) * H + h) * kRecBytes;
     };
-    if (tid == 0 && nc > 0) {
-        mbar_expect_tx(&ms.bar_load[0], kRecBytes);
-        bulk_g2s(sm + kStage0, rec_ptr(0), kRecBytes, &ms.bar_load[0]);
-    }
-    int64_t loads_issued = nc > 0 ? 1 : 0, loads_done = 0;   // uniform / per thread
-    uint32_t mma_issued = 0, mma_done = 0;                    // commits issued / waited
-
-    __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
-    uint32_t mma_parity = 0;
-    bool failed = false;
-    for (int64_t lc = 0; lc < nc; ++lc) {
+    auto stage_addr = [&](int64_t lc) -> uint32_t { return s_base + kStage0 + (uint32_t)(lc & 1) * kStageStride; };
+    auto issue_load = [&](int64_t lc) {
         const int st = (int)(lc & 1);
-        const uint32_t stage = s_base + kStage0 + st * kStageStride;
-        const uint8_t* stage_p = sm + kStage0 + st * kStageStride;
-        if (lc + 1 < nc) {
-            if (tid == 0) {
-                mbar_expect_tx(&ms.bar_load[st ^ 1], kRecBytes);
-                bulk_g2s(sm + kStage0 + (st ^ 1) * kStageStride, rec_ptr(lc + 1), kRecBytes, &ms.bar_load[st ^ 1]);
-            }
-            loads_issued = lc + 2;
-        }
-        bool ok = mbar_wait(&ms.bar_load[st], (uint32_t)((lc >> 1) & 1));
-        if (ok) loads_done = lc + 1;
-        if (ok) mma_issued += 1;
-        if (tid == 0 && ok) {
-            const uint32_t id64 = idesc_bf16(128, 64, false, true);
+        mbar_expect_tx(&ms.bar_load[st], kRecBytes);
+        bulk_g2s(sm + kStage0 + st * kStageStride, rec_ptr(lc), kRecBytes, &ms.bar_load[st]);
+        ld_issued[st] += 1;
+    };
+    const uint32_t id64 = idesc_bf16(128, 64, false, true);
+    const uint32_t id128 = idesc_bf16(128, 128, false, false);
+    // (a) D1 = S^T W^T and (b) D2 = S^T Q~^T for chunk lc
+    auto issue_ab = [&](int64_t lc) {
+        const uint32_t stage = stage_addr(lc);
 #pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks) {
-                const uint64_t ad = sdesc(s_base + kSa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                mma_bf16(tD1, ad, sdesc(stage + kRecW + ks * 2048, 1024, 1024), id64, ks > 0 ? 1u : 0u);
-            }
-            mma_commit(&ms.bar_mma);
-#pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks) {
-                const uint64_t ad = sdesc(s_base + kSa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-                mma_bf16(tD2, ad, sdesc(stage + kRecQ + ks * 2048, 1024, 1024), id64, ks > 0 ? 1u : 0u);
-            }
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint64_t ad = sdesc(s_base + kSa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+            mma_bf16(tD1, ad, sdesc(stage + kRecW + ks * 2048, 1024, 1024), id64, ks > 0 ? 1u : 0u);
         }
-        ok = ok && mbar_wait(&ms.bar_mma, mma_parity);
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint64_t ad = sdesc(s_base + kSa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+            mma_bf16(tD2(lc), ad, sdesc(stage + kRecQ + ks * 2048, 1024, 1024), id64, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&ms.bar_a);
+        a_issued += 1;
+    };
+    // (c) D2 += U^T P^T and (d) D3 = U^T Kbar for chunk lc
+    auto issue_cd = [&](int64_t lc) {
+        const uint32_t stage = stage_addr(lc);
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks) {
+            const uint64_t ad = sdesc(s_base + kUa + ks * 32, 16, 1024);
+            mma_bf16(tD2(lc), ad, sdesc(stage + kRecP + ks * 2048, 1024, 1024), id64, 1u);
+        }
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks) {
+            const uint64_t ad = sdesc(s_base + kUa + ks * 32, 16, 1024);
+            mma_bf16(tD3, ad, sdesc(stage + kRecK + ks * 32, 16, 1024), id128, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&ms.bar_cd);
+        cd_issued += 1;
+    };
+    __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
+    // outputs of chunk lc (its O^T is complete in D2(lc)): this thread's 16 tokens
+    auto store_outputs = [&](int64_t lc) {
+        const int64_t t0 = tb + lc * kC;
+        const int n = (int)(te - t0 < kC ? te - t0 : kC);
+        uint32_t v[16];
+        tmem_ld16(tD2(lc) + lanebase + tq, v);
+        tmem_wait_ld();
+        __nv_bfloat16* orow = og + ((t0 + tq) * H + h) * kD + j;
+        const int64_t ostride = (int64_t)H * kD;
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            if (tq + e < n) orow[e * ostride] = __float2bfloat16_rn(a.scale * __uint_as_float(v[e]));
+    };
+
+    bool ok = true;
+    if (tid == 0 && nc > 0) {
+        issue_load(0);
+        if (nc > 1) issue_load(1);
+        ok = mbar_wait(&ms.bar_load[0], 0);
         if (ok) {
-            mma_parity ^= 1;
-            mma_done += 1;
+            ld_waited[0] = 1;
+            issue_ab(0);
         }
+    }
+    ok = !__syncthreads_or(!ok);
+    for (int64_t lc = 0; lc < nc && ok; ++lc) {
+        const int st = (int)(lc & 1);
+        const uint8_t* stage_p = sm + kStage0 + st * kStageStride;
+        const uint32_t par = (uint32_t)(lc & 1);
+        // the record of chunk lc has landed (thread 0 saw it before issuing (a))
+        ok = mbar_wait(&ms.bar_load[st], (uint32_t)((lc >> 1) & 1)) && mbar_wait(&ms.bar_a, par);
+        if (tid == 0 && ok) a_waited += 1;
         if (__syncthreads_or(!ok)) {
-            failed = true;
+            ok = false;
             break;
         }
         fence_after_sync();
 
-        // (a) epilogue: U^T = U~^T - D1 for this thread's 32 tokens
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        // (a) epilogue: U^T = U~^T - D1 for this thread's 16 tokens
+        {
             uint32_t v[16];
-            tmem_ld16(tD1 + lanebase + 32 * ch + 16 * hf, v);
+            tmem_ld16(tD1 + lanebase + tq, v);
             tmem_wait_ld();
 #pragma unroll
             for (int e8 = 0; e8 < 2; ++e8) {
-                const int cc = 4 * ch + 2 * hf + e8;
+                const int cc = 2 * ch + e8;
                 const uint4 ut = *reinterpret_cast<const uint4*>(stage_p + kRecU + row64_chunk_off(j, cc));
                 const uint32_t uw[4] = {ut.x, ut.y, ut.z, ut.w};
                 uint32_t outw[4];
@@ -172,30 +213,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
+        if (tid == 0) issue_cd(lc);
 
-        if (tid == 0) {
-            const uint32_t id64 = idesc_bf16(128, 64, false, true);
-            const uint32_t id128 = idesc_bf16(128, 128, false, false);
-#pragma unroll
-            for (int ks = 0; ks < kC / 16; ++ks) {
-                const uint64_t ad = sdesc(s_base + kUa + ks * 32, 16, 1024);
-                mma_bf16(tD2, ad, sdesc(stage + kRecP + ks * 2048, 1024, 1024), id64, 1u);
-            }
-#pragma unroll
-            for (int ks = 0; ks < kC / 16; ++ks) {
-                const uint64_t ad = sdesc(s_base + kUa + ks * 32, 16, 1024);
-                mma_bf16(tD3, ad, sdesc(stage + kRecK + ks * 32, 16, 1024), id128, ks > 0 ? 1u : 0u);
-            }
-            mma_commit(&ms.bar_mma);
-        }
-        mma_issued += 1;
-        ok = mbar_wait(&ms.bar_mma, mma_parity);
-        if (ok) {
-            mma_parity ^= 1;
-            mma_done += 1;
-        }
+        // outputs of the previous chunk while (c) and (d) run
+        if (lc > 0) store_outputs(lc - 1);
+
+        ok = mbar_wait(&ms.bar_cd, par);
+        if (tid == 0 && ok) cd_waited += 1;
         if (__syncthreads_or(!ok)) {
-            failed = true;
+            ok = false;
             break;
         }
         fence_after_sync();
@@ -203,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         // (d) epilogue: S <- gamma * S + D3 ; bf16 copy for the next chunk
         const float* gam = reinterpret_cast<const float*>(stage_p + kRecG) + cbase;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < 2; ++q4) {
             uint32_t v[16];
             tmem_ld16(tD3 + lanebase + cbase + 16 * q4, v);
             tmem_wait_ld();
@@ -211,6 +237,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
             for (int e = 0; e < 16; ++e) S[16 * q4 + e] = fmaf(gam[16 * q4 + e], S[16 * q4 + e], __uint_as_float(v[e]));
         }
         write_sa();
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+
+        // stage st is free again: refill it two chunks ahead; start the next chunk
+        if (tid == 0) {
+            if (lc + 2 < nc) issue_load(lc + 2);
+            if (lc + 1 < nc) {
+                const int st1 = st ^ 1;
+                if (mbar_wait(&ms.bar_load[st1], (uint32_t)(((lc + 1) >> 1) & 1))) {
+                    ld_waited[st1] += 1;
+                    issue_ab(lc + 1);
+                }
+            }
+        }
+
+        // snapshot after this chunk, straight from the fp32 registers
         const int64_t t0 = tb + lc * kC;
         const int n = (int)(te - t0 < kC ? te - t0 : kC);
         const int64_t p_end = pos0 + lc * kC + n;
@@ -223,48 +267,35 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
                 if (slot >= 0 && (int64_t)slot < a.n_slots) {
                     float* dst = a.pool + (int64_t)slot * slot_stride + head_off;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
+                    for (int i = 0; i < 32; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
                 } else if (slot != -1 && tid == 0) {
                     flag(p.status, KDA_DEV_BAD_SLOT);
                 }
             }
         }
-        // (c) epilogue: outputs of this thread's 32 tokens
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v[16];
-            tmem_ld16(tD2 + lanebase + 32 * ch + 16 * hf, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int t = 32 * ch + 16 * hf + e;
-                if (t < n) og[((t0 + t) * H + h) * kD + j] = __float2bfloat16_rn(a.scale * __uint_as_float(v[e]));
-            }
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
     }
 
-    if (failed) {
+    if (!ok) {
         // let this CTA's own copies and MMAs in flight land (bounded) before
         // the shared memory and tensor memory are released
         if (tid == 0) {
             flag(p.status, KDA_DEV_WAIT_TIMEOUT);
-            for (int64_t l = loads_done; l < loads_issued; ++l)
-                mbar_wait(&ms.bar_load[l & 1], (uint32_t)((l >> 1) & 1));
-            for (uint32_t m = mma_done; m < mma_issued; ++m, mma_parity ^= 1)
-                mbar_wait(&ms.bar_mma, mma_parity);
+            for (int st = 0; st < 2; ++st)
+                for (uint32_t l = ld_waited[st]; l < ld_issued[st]; ++l) mbar_wait(&ms.bar_load[st], l & 1);
+            for (uint32_t m = a_waited; m < a_issued; ++m) mbar_wait(&ms.bar_a, m & 1);
+            for (uint32_t m = cd_waited; m < cd_issued; ++m) mbar_wait(&ms.bar_cd, m & 1);
         }
-    } else if (a.final_state) {
-        float* dst = a.final_state + (int64_t)seq * slot_stride + head_off;
+    } else {
+        if (nc > 0) store_outputs(nc - 1);
+        if (a.final_state) {
+            float* dst = a.final_state + (int64_t)seq * slot_stride + head_off;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
+            for (int i = 0; i < 32; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
+        }
     }
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
 }  // namespace
