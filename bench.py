@@ -43,6 +43,7 @@ DECODE_CFG = "decode_512x32"
 #   flops: 6 d_k d_v (state products) + C (3 d_k + 2 d_v) (chunk-local) = 139264
 PREFILL_BYTES_PER_TH = 3 * 256 + 512 + 4 + 256 + 256
 PREFILL_FLOPS_PER_TH = 6 * 128 * 128 + 64 * (3 * 128 + 2 * 128)
+CHUNK_RECORD_BYTES = 74240     # one (chunk, head) record between the two prefill stages
 
 
 def decode_bytes(n, H, d):
@@ -133,9 +134,9 @@ def kernel_fingerprint():
     return h.hexdigest()[:16]
 
 
-# DRAM bytes per launch of the dominant prefill kernel from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by the source fingerprint
-# it was taken on; any other fingerprint reports null.
+# DRAM bytes per launch of a prefill kernel on this workload from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (source fingerprint,
+# kernel); any other fingerprint reports null.
 RECORDED_TRAFFIC = {}
 
 
@@ -226,40 +227,65 @@ def bench_ours(args, rank, world, dev, dist_on):
         prefill_once()
     assert kda.kda_check_status(stream) == 0
 
+    # per-kernel timing marks recorded by the library inside every timed step
+    n_marks = 8
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(n_marks)] for _ in range(args.steps)]
+    for evs in marks:
+        for e in evs:
+            e.record(stream)          # create the events before the timed region
+    torch.cuda.synchronize(dev)
+
     # ---- device-resident timed region
     clocks = ClockSampler(dev)
     clocks.start()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    recorded = []
     barrier(dist_on)
     launches0 = kda.kda_launch_count()
-    ev[0].record(stream)
+    ev0.record(stream)
     for i in range(args.steps):
-        prefill_once()
-        ev[i + 1].record(stream)
+        recorded.append(kda.kda_prefill_chunked_events(pargs, marks[i], stream))
+    ev1.record(stream)
     barrier(dist_on)
     launches = kda.kda_launch_count() - launches0
     clk = clocks.stop()
-    step_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), dist_on, dev)
+    total_ms = max_over_ranks(ev0.elapsed_time(ev1), dist_on, dev)
     ms_per_step = total_ms / args.steps
     value = world * total * args.steps / (total_ms / 1e3)
     assert kda.kda_check_status(stream) == 0
 
-    # dominant kernel: the stage timing entry point splits a step by kernel when
-    # the path has several; the token-serial path is one launch per step
-    stage = getattr(kda, "prefill_stage_times", None)
-    stages = stage(pargs, stream) if stage else {"prefill": statistics.mean(step_ms)}
+    stages = {}
+    for rec in recorded:
+        for (name, e_a), (_, e_b) in zip(rec[:-1], rec[1:]):
+            stages[name] = stages.get(name, 0.0) + e_a.elapsed_time(e_b) / args.steps
     dom_name, dom_ms = max(stages.items(), key=lambda kv: kv[1])
     th = total * H
-    alg_bytes = th * PREFILL_BYTES_PER_TH + n * H * d * d * 4
+    path_bytes = th * PREFILL_BYTES_PER_TH + n * H * d * d * 4
     alg_flops = th * PREFILL_FLOPS_PER_TH
+    # the dominant kernel's own algorithmic traffic
+    if dom_name == "chunk_local":
+        n_ch = (T // 64) * n * H
+        dom_bytes = th * (3 * 256 + 512 + 4) + n_ch * CHUNK_RECORD_BYTES
+        dom_note = "reads q, k, v, alpha, beta; writes one 74,240-byte record per (chunk, head)"
+    elif dom_name == "chunk_recur":
+        n_ch = (T // 64) * n * H
+        dom_bytes = n_ch * CHUNK_RECORD_BYTES + th * (256 + 256) + n * H * d * d * 4
+        dom_note = "reads one record per (chunk, head); writes o, snapshots and final states"
+    else:
+        dom_bytes = path_bytes
+        dom_note = "the whole path's algorithmic bytes"
     fp = kernel_fingerprint()
-    traffic = RECORDED_TRAFFIC.get(fp)
+    traffic = RECORDED_TRAFFIC.get((fp, dom_name))
     roofline = {"bound": "hbm", "kernel": dom_name,
-                "achieved": alg_bytes / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": alg_bytes / (dom_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                "achieved": dom_bytes / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": dom_bytes / (dom_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
                 "traffic": traffic, "peak_source": peaks["source"],
-                "algorithmic_bytes_per_launch": alg_bytes}
+                "algorithmic_bytes_per_launch": dom_bytes, "bytes_counted": dom_note,
+                "ms_per_launch": dom_ms}
+    path = {"achieved_gbs": path_bytes / (ms_per_step / 1e3) / 1e9,
+            "frac_of_hbm": path_bytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "algorithmic_bytes_per_step": path_bytes,
+            "bytes_counted": "1796 B per token-head (q, k, v, alpha, beta, o, snapshot share) + final states"}
     tensor = {"achieved_tflops": alg_flops / (ms_per_step / 1e3) / 1e12,
               "peak_tflops": peaks["bf16_tflops"],
               "frac": alg_flops / (ms_per_step / 1e3) / 1e12 / peaks["bf16_tflops"],
@@ -375,9 +401,10 @@ def bench_ours(args, rank, world, dev, dist_on):
         "config": {"workload": f"{PREFILL_CFG}: {n} sequences x {T} tokens, H={H}, d_k=d_v={d}, "
                                "bf16 q/k/v/o, fp32 alpha/beta/state, chunk 64, snapshot every 256 "
                                "tokens into a block-indexed pool, zero initial state",
-                   "l2": f"inputs larger than L2: {alg_bytes / 1e9:.2f} GB of algorithmic traffic per step",
+                   "l2": f"inputs larger than L2: {path_bytes / 1e9:.2f} GB of algorithmic traffic per step",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
+        "path": path,
         "tensor": tensor,
         "stage_ms": stages,
         "e2e": e2e,

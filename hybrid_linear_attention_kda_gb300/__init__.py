@@ -77,6 +77,9 @@ def load():
     lib.kda_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
     lib.kda_prefill_chunked.restype = ctypes.c_int
     lib.kda_prefill_chunked.argtypes = [ctypes.POINTER(PrefillArgs), vp]
+    lib.kda_prefill_chunked_events.restype = ctypes.c_int
+    lib.kda_prefill_chunked_events.argtypes = [ctypes.POINTER(PrefillArgs), vp, ctypes.POINTER(vp), i32,
+                                               ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_char_p)]
     lib.kda_decode_step.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, vp, f32, vp]
     lib.kda_snapshot_gather.restype = ctypes.c_int
@@ -172,6 +175,20 @@ def kda_prefill_workspace_size(args: PrefillArgs) -> int:
 def kda_prefill_chunked(args: PrefillArgs, stream=None):
     """Launch the chunked prefill described by ``args`` on ``stream``."""
     _check(load().kda_prefill_chunked(ctypes.byref(args), _stream_handle(stream)))
+
+
+def kda_prefill_chunked_events(args: PrefillArgs, events, stream=None):
+    """``kda_prefill_chunked`` that also records ``events`` (``torch.cuda.Event``
+    with timing, already recorded once so that they exist) before each of its
+    kernels and after the last.  Returns [(kernel name, event), ...]; the last
+    name is ``"end"``."""
+    n = len(events)
+    arr = (ctypes.c_void_p * n)(*[e.cuda_event for e in events])
+    names = (ctypes.c_char_p * n)()
+    nrec = ctypes.c_int32(0)
+    _check(load().kda_prefill_chunked_events(ctypes.byref(args), _stream_handle(stream), arr, n,
+                                             ctypes.byref(nrec), names))
+    return [(names[i].decode(), events[i]) for i in range(nrec.value)]
 
 
 def kda_decode_step(q, k, v, alpha, beta, pool, state_slot, o, scale=1.0, stream=None):

@@ -172,7 +172,29 @@ size_t kda_prefill_workspace_size(const kda_prefill_args* a) {
     return workspace_bytes_for(a);
 }
 
-kda_status_t kda_prefill_chunked(const kda_prefill_args* a, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Launch the prefill; when marks is non-null, record marks->ev[i] before the
+// i-th kernel and one after the last.
+struct Marks {
+    void* const* ev;
+    int32_t n_ev, n_rec;
+    const char** names;
+};
+
+kda_status_t mark(Marks* m, cudaStream_t s, const char* name) {
+    if (!m) return KDA_OK;
+    if (m->n_rec >= m->n_ev) return fail(KDA_ERR_INVALID_ARG, "kda_prefill_chunked_events: need more events");
+    cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(m->ev[m->n_rec]), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    if (m->names) m->names[m->n_rec] = name;
+    m->n_rec += 1;
+    return KDA_OK;
+}
+
+kda_status_t prefill_impl(const kda_prefill_args* a, void* stream, Marks* m) {
     kda_status_t st = validate_prefill(a);
     if (st != KDA_OK) return st;
     if (a->n_seqs == 0) return KDA_OK;
@@ -188,9 +210,16 @@ kda_status_t kda_prefill_chunked(const kda_prefill_args* a, void* stream) {
     p.a = *a;
     p.chain_flag = nullptr;
     p.status = status;
+#define KDA_MARK(name)                          \
+    do {                                        \
+        kda_status_t ms_ = mark(m, s, name);    \
+        if (ms_ != KDA_OK) return ms_;          \
+    } while (0)
     if (!use_chunked(a)) {
+        KDA_MARK("prefill_token");
         cudaError_t e = kda::launch_prefill_token(p, s);
         if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+        KDA_MARK("end");
         return KDA_OK;
     }
     const WorkspaceLayout w = layout_for(a);
@@ -202,17 +231,41 @@ kda_status_t kda_prefill_chunked(const kda_prefill_args* a, void* stream) {
     c.records = ws + w.records;
     c.max_chunks = max_chunks_for(a);
     c.status = status;
+    KDA_MARK("chunk_meta");
     cudaError_t e = kda::launch_chunk_meta(c, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill meta launch");
+    KDA_MARK("chunk_local");
     e = kda::launch_chunk_local(c, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill chunk-local launch");
+    KDA_MARK("chunk_recur");
     e = kda::launch_chunk_recur(c, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill chunk-recurrence launch");
     // chains whose gates left the factorisation's range: token by token
+    KDA_MARK("prefill_token_fallback");
     p.chain_flag = c.chain_flag;
     e = kda::launch_prefill_token(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill fallback launch");
+    KDA_MARK("end");
+#undef KDA_MARK
     return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_prefill_chunked(const kda_prefill_args* a, void* stream) {
+    return prefill_impl(a, stream, nullptr);
+}
+
+kda_status_t kda_prefill_chunked_events(const kda_prefill_args* a, void* stream, void* const* events,
+                                        int32_t n_events, int32_t* n_recorded, const char** names) {
+    if (n_recorded) *n_recorded = 0;
+    if (!events || n_events <= 0) return fail(KDA_ERR_INVALID_ARG, "events array is empty");
+    Marks m{events, n_events, 0, names};
+    kda_status_t st = prefill_impl(a, stream, &m);
+    if (n_recorded) *n_recorded = m.n_rec;
+    return st;
 }
 
 kda_status_t kda_decode_step(int32_t n_seqs, int32_t n_heads, int32_t d_k, int32_t d_v,

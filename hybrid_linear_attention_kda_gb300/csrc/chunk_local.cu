@@ -1,24 +1,32 @@
 // Stage one of the chunked prefill: everything of a 64-token chunk that does not
-// depend on the carried state, for all (chunk, head) pairs in parallel.
+// depend on the carried state, for all (chunk, head) pairs.
+//
+// A persistent kernel: one CTA per SM walks its share of the (chunk, head) items.
+// The items' q, k, v and alpha tiles ([64 tokens x 128 channels], token rows
+// H*128 elements apart in the packed tensors) arrive by TMA tensor copies into
+// two input stages, so the next item's 80 KiB are in flight while the current
+// item is computed.  Records go straight to the workspace.
 //
 // Decay factors are products of alphas over token ranges (no exp / log): with
-// the chunk split into halves of 32 tokens,
-//   Gamma_r    = prod_{tau <= r} alpha            (chunk prefix, <= 1)
-//   kappa_r    = prod_{tau > r} alpha             (chunk suffix, <= 1)
-//   rho_r      = prod_{32 <= tau <= r} alpha      (r in half 1: exp(g_r - g_31))
-//   sigma_s    = prod_{s < tau <= 31} alpha       (s in half 0: exp(g_31 - g_s))
-//   phi_r      = exp(g_r - g_m) with m the 16th token of r's half, psi = 1/phi.
-// The intra-chunk products A and P come from one tcgen05 MMA whose rows are the
-// key tokens s and whose columns are query / key tokens r:
-//   rows 0..63   k_s psi_s        x  cols 0..63   q_r phi_r    -> P, same half
-//   rows 64..95  k_s sigma_s         cols 64..95  q_r rho_r    -> P, r in half 1, s in half 0
-//                                    cols 96..159 k_r phi_r    -> A, same half
-//                                    cols 160..191 k_r rho_r   -> A, r in half 1, s in half 0
-// Within a half the factors phi, psi span at most 16 tokens; a chunk whose
-// factors leave [2^-100, 2^100] flags its (sequence, head) for the token-serial
-// kernel.  T = (I + A)^-1 is inverted by 16 x 16 blocks in fp32, then W and U~ come
-// from a second MMA (X^T T^T and Y^T T^T with X = diag(beta) Gamma K,
-// Y = diag(beta) V).
+// the chunk split into halves of 32 tokens and m the 16th token of a half,
+//   Gamma_r = prod_{tau <= r} alpha              (chunk prefix, <= 1)
+//   kappa_r = prod_{tau > r} alpha               (chunk suffix, <= 1)
+//   phi_r   = exp(g_r - g_m)                     (own half's reference token)
+//   psi_s   = 1 / phi_s
+//   xi_s    = exp(g_47 - g_s)  for s in half 0   (<= 1)
+// The intra-chunk products A and P come from one tcgen05 MMA (M = N = K = 128)
+// whose rows are key tokens s and whose columns are query / key tokens r:
+//   rows 0..63   k_s psi_s     x  cols 0..63    q_r phi_r   -> P within a half
+//   rows 64..95  k_s xi_s                                  -> P, r in half 1, s in half 0
+//                                 cols 64..127  k_r phi_r   -> A (same rows)
+// For r in half 1, phi_r xi_s = exp(g_r - g_s) exactly; where xi_s underflows the
+// true entry is below 2^-100 * e^-87 relative to the others.  Within a half phi,
+// psi span at most 16 tokens; a chunk whose factors leave [2^-100, 2^100] flags
+// its (sequence, head) for the token-serial kernel.  T = (I + A)^-1 is inverted
+// by 16 x 16 blocks in fp32, then W and U~ come from a second MMA
+// (X^T T^T and Y^T T^T with X = diag(beta) Gamma K, Y = diag(beta) V).
+#include <cuda.h>
+
 #include "chunk_common.cuh"
 
 namespace kda {
@@ -27,30 +35,35 @@ using namespace tc;
 
 constexpr int kThreads = 256;
 // shared memory (1024-aligned base)
-constexpr uint32_t kAPa = 0;            // A/P MMA operand A: MN-major [c][128 rows s]
-constexpr uint32_t kAPb = 32768;        // A/P MMA operand B: MN-major [c][192 cols]
-constexpr uint32_t kLboA = 1024, kSboA = 2048, kLboB = 1024, kSboB = 3072;
-constexpr uint32_t kAmat = 0;           // after the A/P MMA: A fp32 [64][64]
-constexpr uint32_t kTm = 16384;         //   T as MN-major [s][r] bf16
-constexpr uint32_t kXt = 24576;         //   X^T K-major [c][s]
-constexpr uint32_t kYt = 40960;         //   Y^T K-major [j][s]
-constexpr uint32_t kTf = 57344;         //   T fp32 [64][64]
-constexpr uint32_t kTscr = 73728;       //   block-product scratch, 3 x 16 x 16 fp32
-constexpr uint32_t kMisc = 81920;
-constexpr size_t kSmemBytes = kMisc + 2048 + 1024;
+constexpr uint32_t kStageBytes = 81920;    // one input stage
+constexpr uint32_t kSq = 0, kSk = 16384, kSv = 32768, kSal = 49152;   // q, k, v bf16; alpha fp32 [64][128]
+constexpr uint32_t kR = 2 * kStageBytes;   // A/P operands, then A / T scratch
+constexpr uint32_t kAPa = kR;              // MN-major [c][128 rows s]
+constexpr uint32_t kAPb = kR + 32768;      // MN-major [c][128 cols r]
+constexpr uint32_t kLbo = 1024, kSbo = 2048;
+constexpr uint32_t kAmat = kR;             // after the A/P MMA: A fp32 [64][64]
+constexpr uint32_t kTf = kR + 16384;       //   T fp32 [64][64]
+constexpr uint32_t kTscr = kR + 32768;     //   block-product scratch, 3 x 16 x 16 fp32
+constexpr uint32_t kTm = kR + 36864;       //   T^T bf16, MN-major [s][r]
+constexpr uint32_t kMisc = kR + 65536;
+constexpr uint32_t kTmemCols = 128;
 
 struct Misc {
-    float beta[kC];
-    float tot[2][kD];
-    uint64_t bar;
+    float beta[2][kC];
+    uint64_t bar_load[2];
+    uint64_t bar_mma;
     uint32_t tslot;
     int32_t guard_fail;
 };
-static_assert(sizeof(Misc) <= 2048, "misc");
+constexpr size_t kSmemBytes = kMisc + sizeof(Misc) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory");
+
+struct LocalMaps {
+    CUtensorMap q, k, v, alpha;   // 2-D views [T_tot rows x H*128 elements]
+};
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
-
 __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
     return make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
                       pack_bf16(v[6], v[7]));
@@ -58,11 +71,10 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
 __device__ __forceinline__ void sts16(uint32_t saddr, uint4 v) { st_shared_v4(saddr, v.x, v.y, v.z, v.w); }
 __device__ __forceinline__ void stg16(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
-// byte offset of the 16-byte chunk (mn .. mn+7, k) in an MN-major tile
-__device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k, uint32_t lbo, uint32_t sbo) {
-    return (k >> 3) * sbo + (mn >> 6) * lbo + (k & 7u) * 128u + ((((mn & 63u) >> 3) ^ (k & 7u)) << 4);
+// byte offset of the 16-byte chunk (mn .. mn+7, k) of an MN-major tile
+__device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
+    return (k >> 3) * kSbo + (mn >> 6) * kLbo + (k & 7u) * 128u + ((((mn & 63u) >> 3) ^ (k & 7u)) << 4);
 }
-
 
 // T = (I + A)^-1 for a strictly lower triangular 64 x 64 A (fp32, row-major),
 // by 16 x 16 blocks: the four diagonal blocks by forward substitution, then the
@@ -113,7 +125,34 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) chunk_local_kernel(ChunkLaunch p) {
+struct Item {
+    int64_t g;     // global chunk
+    int h;         // head
+    int seq;
+    int64_t t0;    // first packed token of the chunk
+    int n;         // tokens in the chunk
+};
+
+__device__ __forceinline__ Item decode_item(const ChunkLaunch& p, int64_t item) {
+    Item it;
+    const int H = p.a.n_heads;
+    it.g = item / H;
+    it.h = (int)(item % H);
+    int lo = 0, hi = p.a.n_seqs - 1;   // last sequence whose first chunk is <= g
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.chunk_base[mid] <= it.g) lo = mid;
+        else hi = mid - 1;
+    }
+    it.seq = lo;
+    const int64_t tb = p.a.cu_seqlens[lo], te = p.a.cu_seqlens[lo + 1];
+    it.t0 = tb + (it.g - p.chunk_base[lo]) * kC;
+    it.n = (int)(te - it.t0 < kC ? te - it.t0 : kC);
+    return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant__ LocalMaps tm) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Misc& ms = *reinterpret_cast<Misc*>(sm + kMisc);
@@ -122,340 +161,365 @@ __global__ void __launch_bounds__(kThreads, 2) chunk_local_kernel(ChunkLaunch p)
     const kda_prefill_args& a = p.a;
     const int H = a.n_heads;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t g = blockIdx.x / H;
-    const int h = (int)(blockIdx.x % H);
-    const int n_seqs = a.n_seqs;
-    const int64_t total_chunks = p.chunk_base[n_seqs];
-    if (g >= total_chunks || g >= p.max_chunks) return;
-    int lo = 0, hi = n_seqs - 1;   // last sequence whose first chunk is <= g
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.chunk_base[mid] <= g) lo = mid;
-        else hi = mid - 1;
-    }
-    const int seq = lo;
-    int64_t tb, te, pos0;
-    int32_t init;
-    uint32_t bad;
-    if (!seq_valid(a, seq, &tb, &te, &pos0, &init, &bad)) return;
-    const int64_t t0 = tb + (g - p.chunk_base[seq]) * kC;
-    const int n = (int)(te - t0 < kC ? te - t0 : kC);
-    uint8_t* rec = p.records + ((size_t)g * H + h) * kRecBytes;
-    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
-    const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(a.v);
-    const int64_t tstride = (int64_t)H * kD;       // elements between consecutive tokens
-    const int64_t ebase = (t0 * H + h) * kD;       // element (token 0 of the chunk, channel 0)
+    const int64_t total_chunks = p.chunk_base[a.n_seqs] < p.max_chunks ? p.chunk_base[a.n_seqs] : p.max_chunks;
+    const int64_t n_items = total_chunks * H;
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    if (first >= n_items) return;
 
-    // ---------------------------------------------------------------- phase 1: gates, operands
-    if (warp == 0) tmem_alloc(&ms.tslot, 256);
+    if (warp == 0) tmem_alloc(&ms.tslot, kTmemCols);
     if (tid == 0) {
+        mbar_init(&ms.bar_load[0], 1);
+        mbar_init(&ms.bar_load[1], 1);
+        mbar_init(&ms.bar_mma, 1);
         ms.guard_fail = 0;
-        mbar_init(&ms.bar, 1);
         fence_mbar_init();
     }
-    if (tid < kC) ms.beta[tid] = tid < n ? a.beta[(t0 + tid) * H + h] : 0.f;
-
-    const int c = tid & (kD - 1);
-    const int hh = tid >> 7;       // which half of the chunk this thread walks
-    float al[32];
-    uint32_t qp[16], kp[16];
-    {
-        float prod = 1.f;
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            const int r = 32 * hh + i;
-            const int64_t e0 = ebase + (int64_t)r * tstride + c, e1 = e0 + tstride;
-            const bool v0 = r < n, v1 = r + 1 < n;
-            al[i] = v0 ? a.alpha[e0] : 1.f;
-            al[i + 1] = v1 ? a.alpha[e1] : 1.f;
-            const uint32_t q0 = v0 ? __bfloat16_as_ushort(qg[e0]) : 0u, q1 = v1 ? __bfloat16_as_ushort(qg[e1]) : 0u;
-            const uint32_t k0 = v0 ? __bfloat16_as_ushort(kg[e0]) : 0u, k1 = v1 ? __bfloat16_as_ushort(kg[e1]) : 0u;
-            qp[i >> 1] = q0 | (q1 << 16);
-            kp[i >> 1] = k0 | (k1 << 16);
-            prod *= al[i];
-            prod *= al[i + 1];
-        }
-        ms.tot[hh][c] = prod;
-    }
+    // thread 0 issues every copy and MMA and counts them, to drain on a timeout
+    uint32_t ld_issued[2] = {0, 0}, ld_waited[2] = {0, 0}, mma_issued = 0, mma_waited = 0;
+    auto issue_load = [&](int64_t item, int st) {
+        const Item it = decode_item(p, item);
+        uint8_t* S = sm + st * kStageBytes;
+        mbar_expect_tx(&ms.bar_load[st], kStageBytes);
+        const int32_t x = it.h * kD, y = (int32_t)it.t0;
+        tma_load_2d(S + kSq, &tm.q, x, y, &ms.bar_load[st]);
+        tma_load_2d(S + kSk, &tm.k, x, y, &ms.bar_load[st]);
+        tma_load_2d(S + kSv, &tm.v, x, y, &ms.bar_load[st]);
+        tma_load_2d(S + kSal, &tm.alpha, x, y, &ms.bar_load[st]);
+        ld_issued[st] += 1;
+    };
+    // beta of an item, one token per thread tid < 64
+    auto load_beta = [&](int64_t item) -> float {
+        if (tid >= kC || item >= n_items) return 0.f;
+        const Item it = decode_item(p, item);
+        return tid < it.n ? a.beta[(it.t0 + tid) * H + it.h] : 0.f;
+    };
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = ms.tslot;
-    const float H0 = ms.tot[0][c], H1 = ms.tot[1][c];
-    if (hh == 1) reinterpret_cast<float*>(rec + kRecG)[c] = H0 * H1;
+    if (tid == 0) {
+        issue_load(first, 0);
+        if (first + step < n_items) issue_load(first + step, 1);
+    }
+    if (tid < kC) ms.beta[0][tid] = load_beta(first);
+    float beta_next = load_beta(first + step);
+    __syncthreads();
 
-    bool guard_bad = false;
+    const int c = tid & (kD - 1);
+    const int hh = tid >> 7;       // which half of the chunk this thread walks
+    const uint32_t lanebase = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t apa = s_base + kAPa, apb = s_base + kAPb;
-    // Each walk below keeps one running product; splitting the walks keeps only
-    // a few 8-token staging groups live at a time.
-    {   // forward: Gamma (Q~ to the record), rho (half 1: q rho, k rho)
-        float P = 1.f;
-        float gq[8], oq[8], ok[8];
+    bool ok = true;
+    int k = 0;
+    for (int64_t item = first; item < n_items; item += step, ++k) {
+        const int st = k & 1;
+        const Item it = decode_item(p, item);
+        const int n = it.n;
+        uint8_t* rec = p.records + ((size_t)it.g * H + it.h) * kRecBytes;
+        const uint8_t* S = sm + st * kStageBytes;
+        const uint32_t Ss = s_base + st * kStageBytes;
+        const float* bsm = ms.beta[st];
+
+        ok = mbar_wait(&ms.bar_load[st], (uint32_t)((k >> 1) & 1));
+        if (tid == 0 && ok) ld_waited[st] += 1;
+        if (__syncthreads_or(!ok)) {
+            ok = false;
+            break;
+        }
+
+        // ------------------------------------------------------------ phase 1: gates, operands
+        const float* sal = reinterpret_cast<const float*>(S + kSal);
+        const uint16_t* sq = reinterpret_cast<const uint16_t*>(S + kSq);
+        const uint16_t* sk = reinterpret_cast<const uint16_t*>(S + kSk);
+        float al[32];
+        uint32_t qp[16], kp[16];
+        float own = 1.f;
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const int r = 32 * hh + i;
+            const bool v0 = r < n, v1 = r + 1 < n;
+            al[i] = v0 ? sal[r * kD + c] : 1.f;
+            al[i + 1] = v1 ? sal[(r + 1) * kD + c] : 1.f;
+            qp[i >> 1] = (v0 ? (uint32_t)sq[r * kD + c] : 0u) | ((v1 ? (uint32_t)sq[(r + 1) * kD + c] : 0u) << 16);
+            kp[i >> 1] = (v0 ? (uint32_t)sk[r * kD + c] : 0u) | ((v1 ? (uint32_t)sk[(r + 1) * kD + c] : 0u) << 16);
+            own *= al[i];
+            own *= al[i + 1];
+        }
+        // the other half's product; for half 0 also the product over tokens 32..47
+        float oth = 1.f, mid = 1.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
-            const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-            P *= al[i];
-            gq[i & 7] = qf * (hh ? H0 * P : P);
-            oq[i & 7] = qf * P;
-            ok[i & 7] = kf * P;
-            if ((i & 7) == 7) {
-                const uint32_t r0 = 32 * hh + (i & ~7);
-                stg16(rec + kRecQ + row64_chunk_off(c, r0 >> 3), pack8(gq));
-                if (hh) {
-                    sts16(apb + mn_chunk(64 + (i & ~7), c, kLboB, kSboB), pack8(oq));
-                    sts16(apb + mn_chunk(160 + (i & ~7), c, kLboB, kSboB), pack8(ok));
+            const int r = 32 * (1 - hh) + i;
+            oth *= r < n ? sal[r * kD + c] : 1.f;
+            if (i == 15) mid = oth;
+        }
+        const float H0 = hh ? oth : own, H1 = hh ? own : oth;
+        if (hh == 1) reinterpret_cast<float*>(rec + kRecG)[c] = H0 * H1;
+
+        bool guard_bad = false;
+        {   // forward: Gamma (Q~ to the record)
+            float P = 1.f;
+            float gq[8];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
+                P *= al[i];
+                gq[i & 7] = qf * (hh ? H0 * P : P);
+                if ((i & 7) == 7) stg16(rec + kRecQ + row64_chunk_off(c, (32 * hh + (i & ~7)) >> 3), pack8(gq));
+            }
+        }
+        {   // forward from the half's reference token: phi = E, psi = 1/E (local tokens 16..31)
+            float E = 1.f;
+            float dq[8], dk[8], dd[8];
+#pragma unroll
+            for (int i = 16; i < 32; ++i) {
+                const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
+                const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+                E *= al[i];
+                guard_bad |= !(E >= kGuardMin);
+                const float inv = __fdividef(1.f, E);
+                dq[i & 7] = qf * E;
+                dk[i & 7] = kf * E;
+                dd[i & 7] = kf * inv;
+                if ((i & 7) == 7) {
+                    const uint32_t r0 = 32 * hh + (i & ~7);
+                    sts16(apb + mn_chunk(r0, c), pack8(dq));
+                    sts16(apb + mn_chunk(64 + r0, c), pack8(dk));
+                    sts16(apa + mn_chunk(r0, c), pack8(dd));
                 }
             }
         }
-    }
-    {   // forward from the half's reference token: phi = E, psi = 1/E (local tokens 16..31)
-        float E = 1.f;
-        float dq[8], dk[8], dd[8];
+        {   // backward: kappa (Kbar to the record); half 0 also xi = exp(g_47 - g_s)
+            float Q = 1.f;
+            float kb[8], kx[8];
 #pragma unroll
-        for (int i = 16; i < 32; ++i) {
-            const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
-            const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-            E *= al[i];
-            guard_bad |= !(E >= kGuardMin);
-            const float inv = __fdividef(1.f, E);
-            dq[i & 7] = qf * E;
-            dk[i & 7] = kf * E;
-            dd[i & 7] = kf * inv;
-            if ((i & 7) == 7) {
-                const uint32_t r0 = 32 * hh + (i & ~7);
-                sts16(apb + mn_chunk(r0, c, kLboB, kSboB), pack8(dq));
-                sts16(apb + mn_chunk(96 + r0, c, kLboB, kSboB), pack8(dk));
-                sts16(apa + mn_chunk(r0, c, kLboA, kSboA), pack8(dd));
+            for (int i = 31; i >= 0; --i) {
+                const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+                kb[i & 7] = kf * (hh ? Q : Q * H1);
+                kx[i & 7] = kf * (Q * mid);
+                if ((i & 7) == 0) {
+                    stg16(rec + kRecK + row64_chunk_off(c, (32 * hh + i) >> 3), pack8(kb));
+                    if (!hh) sts16(apa + mn_chunk(64 + i, c), pack8(kx));
+                }
+                Q *= al[i];
             }
         }
-    }
-    {   // backward: kappa (Kbar to the record), sigma (half 0: k sigma); zero pad rows
-        float Q = 1.f;
-        float kb[8], kc[8];
+        {   // backward to the half's reference token: phi = 1/D, psi = D (local tokens 0..15)
+            float Dd = 1.f;
+            float dq[8], dk[8], dd[8];
 #pragma unroll
-        for (int i = 31; i >= 0; --i) {
-            const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-            kb[i & 7] = kf * (hh ? Q : Q * H1);
-            kc[i & 7] = kf * Q;
-            if ((i & 7) == 0) {
-                const uint32_t r0 = 32 * hh + i;
-                stg16(rec + kRecK + row64_chunk_off(c, r0 >> 3), pack8(kb));
-                if (!hh) sts16(apa + mn_chunk(64 + i, c, kLboA, kSboA), pack8(kc));
-                else sts16(apa + mn_chunk(96 + i, c, kLboA, kSboA), make_uint4(0u, 0u, 0u, 0u));
+            for (int i = 15; i >= 0; --i) {
+                const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
+                const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+                guard_bad |= !(Dd >= kGuardMin);
+                const float inv = __fdividef(1.f, Dd);
+                dq[i & 7] = qf * inv;
+                dk[i & 7] = kf * inv;
+                dd[i & 7] = kf * Dd;
+                if ((i & 7) == 0) {
+                    const uint32_t r0 = 32 * hh + i;
+                    sts16(apb + mn_chunk(r0, c), pack8(dq));
+                    sts16(apb + mn_chunk(64 + r0, c), pack8(dk));
+                    sts16(apa + mn_chunk(r0, c), pack8(dd));
+                }
+                Dd *= al[i];
             }
-            Q *= al[i];
         }
-    }
-    {   // backward to the half's reference token: phi = 1/D, psi = D (local tokens 0..15)
-        float Dd = 1.f;
-        float dq[8], dk[8], dd[8];
-#pragma unroll
-        for (int i = 15; i >= 0; --i) {
-            const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
-            const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-            guard_bad |= !(Dd >= kGuardMin);
-            const float inv = __fdividef(1.f, Dd);
-            dq[i & 7] = qf * inv;
-            dk[i & 7] = kf * inv;
-            dd[i & 7] = kf * Dd;
-            if ((i & 7) == 0) {
-                const uint32_t r0 = 32 * hh + i;
-                sts16(apb + mn_chunk(r0, c, kLboB, kSboB), pack8(dq));
-                sts16(apb + mn_chunk(96 + r0, c, kLboB, kSboB), pack8(dk));
-                sts16(apa + mn_chunk(r0, c, kLboA, kSboA), pack8(dd));
-            }
-            Dd *= al[i];
-        }
-    }
-    if (guard_bad) atomicOr(&ms.guard_fail, 1);
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
+        if (guard_bad) atomicOr(&ms.guard_fail, 1);
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
 
-    if (tid == 0) {
-        if (ms.guard_fail) atomicOr(&p.chain_flag[(int64_t)seq * H + h], 1);
-        const uint32_t idesc = idesc_bf16(128, 192, true, true);
+        if (tid == 0) {
+            if (ms.guard_fail) {
+                atomicOr(&p.chain_flag[(int64_t)it.seq * H + it.h], 1);
+                ms.guard_fail = 0;
+            }
+            const uint32_t idesc = idesc_bf16(128, 128, true, true);
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-            const uint64_t ad = sdesc(apa + ks * 2 * kSboA, kLboA, kSboA);
-            const uint64_t bd = sdesc(apb + ks * 2 * kSboB, kLboB, kSboB);
-            mma_bf16(tbase, ad, bd, idesc, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < kD / 16; ++ks)
+                mma_bf16(tbase, sdesc(apa + ks * 2 * kSbo, kLbo, kSbo), sdesc(apb + ks * 2 * kSbo, kLbo, kSbo), idesc,
+                         ks > 0 ? 1u : 0u);
+            mma_commit(&ms.bar_mma);
+            mma_issued += 1;
         }
-        mma_commit(&ms.bar);
-    }
-    bool ok = mbar_wait(&ms.bar, 0);
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) flag(p.status, KDA_DEV_WAIT_TIMEOUT);
-        if (warp == 0) tmem_dealloc(tbase, 256);
-        return;
-    }
-    fence_after_sync();
+        ok = mbar_wait(&ms.bar_mma, 0);
+        if (tid == 0 && ok) mma_waited += 1;
+        if (__syncthreads_or(!ok)) {
+            ok = false;
+            break;
+        }
+        fence_after_sync();
 
-    // ---------------------------------------------------------------- phase 2: P to the record, A to smem
-    const uint32_t lanebase = (uint32_t)(32 * (warp & 3)) << 16;
-    if (warp < 3) {
-        const int s = warp == 2 ? lane : lane + 32 * warp;      // key token of this TMEM lane
-        const int col0 = 32 * warp;
+        // ------------------------------------------------------------ phase 2: P to the record, A to smem
+        if (warp < 3) {
+            const int s = warp == 2 ? lane : lane + 32 * warp;      // key token of this TMEM lane
+            const int col0 = warp == 0 ? 0 : 32;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v[16];
-            tmem_ld16(tbase + lanebase + col0 + 16 * hf, v);
-            tmem_wait_ld();
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t v[16];
+                tmem_ld16(tbase + lanebase + col0 + 16 * hf, v);
+                tmem_wait_ld();
 #pragma unroll
-            for (int e8 = 0; e8 < 2; ++e8) {
+                for (int e8 = 0; e8 < 2; ++e8) {
+                    const int r0 = col0 + 16 * hf + 8 * e8;
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        x[e] = (warp == 2 || r0 + e >= s) ? __uint_as_float(v[8 * e8 + e]) : 0.f;
+                    stg16(rec + kRecP + row64_chunk_off(s, r0 >> 3), pack8(x));
+                }
+            }
+            if (warp == 1) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) stg16(rec + kRecP + row64_chunk_off(s, cc), make_uint4(0u, 0u, 0u, 0u));
+            }
+        } else if (warp >= 4 && warp < 7) {
+            const int wq = warp - 4;
+            const int s = wq == 2 ? lane : lane + 32 * wq;
+            const int col0 = wq == 0 ? 64 : 96;                     // columns 64 + r
+            float* Am = reinterpret_cast<float*>(sm + kAmat);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t v[16];
+                tmem_ld16(tbase + lanebase + col0 + 16 * hf, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int r = col0 - 64 + 16 * hf + e;
+                    Am[r * kC + s] = (wq == 2 || r > s) ? bsm[r] * __uint_as_float(v[e]) : 0.f;
+                }
+            }
+            if (wq == 1) {
+                for (int r = 0; r < 32; ++r) Am[r * kC + s] = 0.f;
+            }
+        }
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+
+        // ------------------------------------------------------------ phase 3: X^T, Y^T, T
+        uint32_t vq[16];
+        {
+            const uint16_t* sv = reinterpret_cast<const uint16_t*>(S + kSv);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const int r = 32 * hh + i;
+                vq[i >> 1] = (r < n ? (uint32_t)sv[r * kD + c] : 0u) | ((r + 1 < n ? (uint32_t)sv[(r + 1) * kD + c] : 0u) << 16);
+            }
+            // X^T row c (beta_r Gamma_rc k_rc) into the stage's q tile, which is no longer read
+            float Gm = hh ? H0 : 1.f;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int col = col0 + 16 * hf + 8 * e8 + e;
-                    const int r = warp == 2 ? 32 + (col - 64) : col;
-                    const float d = __uint_as_float(v[8 * e8 + e]);
-                    x[e] = (warp == 2 || r >= s) ? d : 0.f;
+                    const int i = 8 * cc + e;
+                    Gm *= al[i];
+                    const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+                    x[e] = bsm[32 * hh + i] * kf * Gm;
                 }
-                const int r0 = warp == 2 ? 32 + 16 * hf + 8 * e8 : col0 + 16 * hf + 8 * e8;
-                stg16(rec + kRecP + row64_chunk_off(s, r0 >> 3), pack8(x));
+                sts16(Ss + kSq + row64_chunk_off(c, 4 * hh + cc), pack8(x));
             }
         }
-        if (warp == 1) {
+        __syncthreads();   // every thread holds its v column: the v tile can be overwritten
+        {   // Y^T row c (beta_r v_rc) into the stage's v tile
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) stg16(rec + kRecP + row64_chunk_off(s, cc), make_uint4(0u, 0u, 0u, 0u));
-        }
-    } else if (warp >= 4 && warp < 7) {
-        const int wq = warp - 4;
-        const int s = wq == 2 ? lane : lane + 32 * wq;
-        const int col0 = wq == 0 ? 96 : (wq == 1 ? 128 : 160);
-        const int rbase = wq == 0 ? 0 : 32;
-        float* Am = reinterpret_cast<float*>(sm + kAmat);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v[16];
-            tmem_ld16(tbase + lanebase + col0 + 16 * hf, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int r = rbase + 16 * hf + e;
-                const float d = __uint_as_float(v[e]);
-                Am[r * kC + s] = (wq == 2 || r > s) ? ms.beta[r] * d : 0.f;
-            }
-        }
-        if (wq == 1) {
-            for (int r = 0; r < 32; ++r) Am[r * kC + s] = 0.f;
-        }
-    }
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-
-    // ---------------------------------------------------------------- phase 3: X^T, Y^T, T
-    // X^T / Y^T rows from this thread's 32 tokens of channel c (two rounds of 16
-    // tokens, to bound the loads in flight per thread), then T.
-    {
-        float Gm = hh ? ms.tot[0][c] : 1.f;
-#pragma unroll 1
-        for (int rnd = 0; rnd < 2; ++rnd) {
-            float ax[16];
-            uint32_t kq[8], vq[8];
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-                const int r = 32 * hh + 16 * rnd + i;
-                const int64_t e0 = ebase + (int64_t)r * tstride + c, e1 = e0 + tstride;
-                const bool v0 = r < n, v1 = r + 1 < n;
-                ax[i] = v0 ? a.alpha[e0] : 1.f;
-                ax[i + 1] = v1 ? a.alpha[e1] : 1.f;
-                kq[i >> 1] = (v0 ? (uint32_t)__bfloat16_as_ushort(kg[e0]) : 0u) |
-                             ((v1 ? (uint32_t)__bfloat16_as_ushort(kg[e1]) : 0u) << 16);
-                vq[i >> 1] = (v0 ? (uint32_t)__bfloat16_as_ushort(vg[e0]) : 0u) |
-                             ((v1 ? (uint32_t)__bfloat16_as_ushort(vg[e1]) : 0u) << 16);
-            }
-            // X^T row c: beta_r Gamma_rc k_rc ;  Y^T row c: beta_r v_rc
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                float x[8], y[8];
+            for (int cc = 0; cc < 4; ++cc) {
+                float y[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * c2 + e;
-                    const float b = ms.beta[32 * hh + 16 * rnd + i];
-                    Gm *= ax[i];
-                    const float kf = (i & 1) ? bf_hi(kq[i >> 1]) : bf_lo(kq[i >> 1]);
+                    const int i = 8 * cc + e;
                     const float vf = (i & 1) ? bf_hi(vq[i >> 1]) : bf_lo(vq[i >> 1]);
-                    x[e] = b * kf * Gm;
-                    y[e] = b * vf;
+                    y[e] = bsm[32 * hh + i] * vf;
                 }
-                const int cc = 4 * hh + 2 * rnd + c2;
-                sts16(s_base + kXt + row64_chunk_off(c, cc), pack8(x));
-                sts16(s_base + kYt + row64_chunk_off(c, cc), pack8(y));
+                sts16(Ss + kSv + row64_chunk_off(c, 4 * hh + cc), pack8(y));
             }
         }
-    }
-    invert_unit_lower(reinterpret_cast<const float*>(sm + kAmat), reinterpret_cast<float*>(sm + kTf),
-                      reinterpret_cast<float*>(sm + kTscr), tid);
-    {
-        // T^T row s (= column s of T, zero above the diagonal) as the MN-major [s][r] operand
-        const float* Tf = reinterpret_cast<const float*>(sm + kTf);
-        const int srow = tid >> 2;
+        invert_unit_lower(reinterpret_cast<const float*>(sm + kAmat), reinterpret_cast<float*>(sm + kTf),
+                          reinterpret_cast<float*>(sm + kTscr), tid);
+        {   // T^T row s (= column s of T, zero above the diagonal) as the MN-major [s][r] operand
+            const float* Tf = reinterpret_cast<const float*>(sm + kTf);
+            const int srow = tid >> 2;
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-            const int cc = 2 * (tid & 3) + q2;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int r = 8 * cc + e;
-                x[e] = r >= srow ? Tf[r * kC + srow] : 0.f;
-            }
-            sts16(s_base + kTm + row64_chunk_off(srow, cc), pack8(x));
-        }
-    }
-    fence_async_smem();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-
-    if (tid == 0) {
-        const uint32_t idesc = idesc_bf16(128, 64, false, true);
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks) {
-            const uint64_t bd = sdesc(s_base + kTm + ks * 2048, 1024, 1024);
-            mma_bf16(tbase, sdesc(s_base + kXt + ks * 32, 16, 1024), bd, idesc, ks > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks) {
-            const uint64_t bd = sdesc(s_base + kTm + ks * 2048, 1024, 1024);
-            mma_bf16(tbase + 64, sdesc(s_base + kYt + ks * 32, 16, 1024), bd, idesc, ks > 0 ? 1u : 0u);
-        }
-        mma_commit(&ms.bar);
-    }
-    ok = mbar_wait(&ms.bar, 1);
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) flag(p.status, KDA_DEV_WAIT_TIMEOUT);
-        if (warp == 0) tmem_dealloc(tbase, 256);
-        return;
-    }
-    fence_after_sync();
-
-    // ---------------------------------------------------------------- phase 4: W and U~ to the record
-    {
-        const int row = 32 * (warp & 3) + lane;
-        const uint32_t col0 = warp < 4 ? 0u : 64u;
-        uint8_t* dst = rec + (warp < 4 ? kRecW : kRecU);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t v[16];
-            tmem_ld16(tbase + lanebase + col0 + 16 * q4, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e8 = 0; e8 < 2; ++e8) {
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int cc = 2 * (tid & 3) + q2;
                 float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * e8 + e]);
-                stg16(dst + row64_chunk_off(row, 2 * q4 + e8), pack8(x));
+                for (int e = 0; e < 8; ++e) {
+                    const int r = 8 * cc + e;
+                    x[e] = r >= srow ? Tf[r * kC + srow] : 0.f;
+                }
+                sts16(s_base + kTm + row64_chunk_off(srow, cc), pack8(x));
             }
         }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16(128, 64, false, true);
+#pragma unroll
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tbase, sdesc(Ss + kSq + ks * 32, 16, 1024), sdesc(s_base + kTm + ks * 2048, 1024, 1024),
+                         idesc, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tbase + 64, sdesc(Ss + kSv + ks * 32, 16, 1024), sdesc(s_base + kTm + ks * 2048, 1024, 1024),
+                         idesc, ks > 0 ? 1u : 0u);
+            mma_commit(&ms.bar_mma);
+            mma_issued += 1;
+        }
+        ok = mbar_wait(&ms.bar_mma, 1);
+        if (tid == 0 && ok) mma_waited += 1;
+        if (__syncthreads_or(!ok)) {
+            ok = false;
+            break;
+        }
+        fence_after_sync();
+        // this stage is no longer read: fetch the item two steps ahead into it
+        if (tid == 0 && item + 2 * step < n_items) issue_load(item + 2 * step, st);
+
+        // ------------------------------------------------------------ phase 4: W and U~ to the record
+        {
+            const int row = 32 * (warp & 3) + lane;
+            const uint32_t col0 = warp < 4 ? 0u : 64u;
+            uint8_t* dst = rec + (warp < 4 ? kRecW : kRecU);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t v[16];
+                tmem_ld16(tbase + lanebase + col0 + 16 * q4, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e8 = 0; e8 < 2; ++e8) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * e8 + e]);
+                    stg16(dst + row64_chunk_off(row, 2 * q4 + e8), pack8(x));
+                }
+            }
+        }
+        // beta of the next item into its buffer; start loading the one after
+        if (tid < kC) ms.beta[st ^ 1][tid] = beta_next;
+        beta_next = load_beta(item + 2 * step);
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    }
+
+    if (!ok && tid == 0) {
+        // let this CTA's own copies and MMAs in flight land (bounded) before
+        // shared and tensor memory are released
+        flag(p.status, KDA_DEV_WAIT_TIMEOUT);
+        for (int st = 0; st < 2; ++st)
+            for (uint32_t l = ld_waited[st]; l < ld_issued[st]; ++l) mbar_wait(&ms.bar_load[st], l & 1);
+        for (uint32_t m = mma_waited; m < mma_issued; ++m) mbar_wait(&ms.bar_mma, m & 1);
     }
     fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
 // ---------------------------------------------------------------- meta: chunk table
@@ -524,14 +588,64 @@ cudaError_t launch_chunk_meta(const ChunkLaunch& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// [rows x cols] row-major tensor, boxes of 64 rows x 128 elements, no swizzle;
+// rows past the end read as zero.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* base, int64_t rows,
+              int64_t cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kC};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_chunk_local(const ChunkLaunch& p, cudaStream_t s) {
-    const int64_t blocks = p.max_chunks * p.a.n_heads;
-    if (blocks == 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(chunk_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    const int64_t max_items = p.max_chunks * p.a.n_heads;
+    if (max_items == 0 || p.a.total_tokens == 0) return cudaSuccess;
+    LocalMaps tm;
+    const int64_t rows = p.a.total_tokens, cols = (int64_t)p.a.n_heads * kD;
+    if (!make_map(&tm.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a.q, rows, cols) ||
+        !make_map(&tm.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a.k, rows, cols) ||
+        !make_map(&tm.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a.v, rows, cols) ||
+        !make_map(&tm.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.a.alpha, rows, cols))
+        return cudaErrorInvalidValue;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(chunk_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = max_items < sms ? max_items : sms;
     note_launch();
-    chunk_local_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(p);
+    chunk_local_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(p, tm);
     return cudaGetLastError();
 }
 

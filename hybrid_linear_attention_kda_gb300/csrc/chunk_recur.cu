@@ -118,35 +118,39 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     };
     const uint32_t id64 = idesc_bf16(128, 64, false, true);
     const uint32_t id128 = idesc_bf16(128, 128, false, false);
-    // (a) D1 = S^T W^T and (b) D2 = S^T Q~^T for chunk lc
+    // Descriptors are built once; a k-step only moves the start address, which
+    // is the low 14-bit field (address >> 4; every operand here lies below
+    // 256 KiB, so adding the step never carries out of the field).
+    const uint64_t dSa = sdesc(s_base + kSa, 16, 1024);
+    const uint64_t dUa = sdesc(s_base + kUa, 16, 1024);
+    const uint64_t dMN = sdesc(0, 1024, 1024);       // MN-major record tile, start added per use
+    const uint64_t dKM = sdesc(0, 16, 1024);         // K-major record tile
+    auto at = [](uint64_t desc, uint32_t byte_off) -> uint64_t { return desc + (uint64_t)(byte_off >> 4); };
+    // (a) D1 = S^T W^T (own commit: the U epilogue waits only for it) and
+    // (b) D2 = S^T Q~^T for chunk lc
     auto issue_ab = [&](int64_t lc) {
         const uint32_t stage = stage_addr(lc);
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-            const uint64_t ad = sdesc(s_base + kSa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-            mma_bf16(tD1, ad, sdesc(stage + kRecW + ks * 2048, 1024, 1024), id64, ks > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-            const uint64_t ad = sdesc(s_base + kSa + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-            mma_bf16(tD2(lc), ad, sdesc(stage + kRecQ + ks * 2048, 1024, 1024), id64, ks > 0 ? 1u : 0u);
-        }
+        for (int ks = 0; ks < kD / 16; ++ks)
+            mma_bf16(tD1, at(dSa, (ks >> 2) * 16384 + (ks & 3) * 32), at(dMN, stage + kRecW + ks * 2048), id64,
+                     ks > 0 ? 1u : 0u);
         mma_commit(&ms.bar_a);
         a_issued += 1;
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks)
+            mma_bf16(tD2(lc), at(dSa, (ks >> 2) * 16384 + (ks & 3) * 32), at(dMN, stage + kRecQ + ks * 2048), id64,
+                     ks > 0 ? 1u : 0u);
     };
-    // (c) D2 += U^T P^T and (d) D3 = U^T Kbar for chunk lc
+    // (c) D2 += U^T P^T and (d) D3 = U^T Kbar for chunk lc; the commit also
+    // covers (b)
     auto issue_cd = [&](int64_t lc) {
         const uint32_t stage = stage_addr(lc);
 #pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks) {
-            const uint64_t ad = sdesc(s_base + kUa + ks * 32, 16, 1024);
-            mma_bf16(tD2(lc), ad, sdesc(stage + kRecP + ks * 2048, 1024, 1024), id64, 1u);
-        }
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tD2(lc), at(dUa, ks * 32), at(dMN, stage + kRecP + ks * 2048), id64, 1u);
 #pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks) {
-            const uint64_t ad = sdesc(s_base + kUa + ks * 32, 16, 1024);
-            mma_bf16(tD3, ad, sdesc(stage + kRecK + ks * 32, 16, 1024), id128, ks > 0 ? 1u : 0u);
-        }
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tD3, at(dUa, ks * 32), at(dKM, stage + kRecK + ks * 32), id128, ks > 0 ? 1u : 0u);
         mma_commit(&ms.bar_cd);
         cd_issued += 1;
     };

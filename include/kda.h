@@ -144,6 +144,19 @@ size_t kda_prefill_workspace_size(const kda_prefill_args *args);
 kda_status_t kda_prefill_chunked(const kda_prefill_args *args, void *stream);
 
 /*
+ * kda_prefill_chunked with timing marks: on `stream`, records events[i] before
+ * the i-th kernel of the prefill and one more after the last, for at most
+ * n_events events (cudaEvent_t handles created by the caller, timing enabled).
+ * *n_recorded receives the number recorded (kernels + 1) and names[i] (when
+ * names is non-NULL, room for n_events entries) the static name of the kernel
+ * that starts at events[i].  For measurement; the results equal those of
+ * kda_prefill_chunked.
+ */
+kda_status_t kda_prefill_chunked_events(const kda_prefill_args *args, void *stream,
+                                        void *const *events, int32_t n_events,
+                                        int32_t *n_recorded, const char **names);
+
+/*
  * One decode step for n_seqs sequences, one token each ("Kimi K3 Tech Intro",
  * section 4.1: the recurrent update of the fused decode kernel, with the state
  * updated in place).  Sequence s reads and rewrites the H states in pool slot
