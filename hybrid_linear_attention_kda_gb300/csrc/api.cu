@@ -146,6 +146,8 @@ std::atomic<uint64_t> g_launches{0};
 
 void kda::note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+kda_status_t kda::record_error(kda_status_t status, const char* message) { return fail(status, "%s", message); }
+
 extern "C" {
 
 uint64_t kda_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -33,6 +33,9 @@ __device__ __forceinline__ void flag(uint32_t* status, uint32_t bit) {
 // Counts kernel launches (kda_launch_count); every launcher calls it once per launch.
 void note_launch(int n = 1);
 
+// Records `message` as this host thread's last error (kda_last_error) and returns status.
+kda_status_t record_error(kda_status_t status, const char* message);
+
 // ----------------------------------------------------------------- launchers
 // Each returns the cudaError_t of its launch.  Arguments were validated by the
 // C-ABI layer.

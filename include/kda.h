@@ -157,6 +157,21 @@ kda_status_t kda_prefill_chunked_events(const kda_prefill_args *args, void *stre
                                         int32_t *n_recorded, const char **names);
 
 /*
+ * kda_prefill_chunked for callers that cannot allocate device memory: the same
+ * arguments (args->workspace and args->workspace_bytes are ignored), with the
+ * prefill's scratch taken from a 64 MiB array in the library's own static device
+ * memory, which every GPU that loads the library holds until process exit.  The
+ * paper has no counterpart to this call; it exists for serving code whose device
+ * memory is all reserved up front, or that may not allocate on its latency
+ * path.  Allocates nothing.  Returns KDA_ERR_UNSUPPORTED when
+ * kda_prefill_workspace_size(args) exceeds 64 MiB.  All calls share the array:
+ * calls that overlap on the GPU race on it.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) and should come before any
+ * stream capture.
+ */
+kda_status_t kda_prefill_chunked_noalloc(const kda_prefill_args *args, void *stream);
+
+/*
  * One decode step for n_seqs sequences, one token each ("Kimi K3 Tech Intro",
  * section 4.1: the recurrent update of the fused decode kernel, with the state
  * updated in place).  Sequence s reads and rewrites the H states in pool slot
