@@ -120,7 +120,7 @@ int64_t max_chunks_for(const kda_prefill_args* a) {
 }
 
 struct WorkspaceLayout {
-    size_t chunk_base, chain_flag, records, total;
+    size_t chunk_base, chain_flag, chunk_info, records, total;
 };
 
 WorkspaceLayout layout_for(const kda_prefill_args* a) {
@@ -131,6 +131,8 @@ WorkspaceLayout layout_for(const kda_prefill_args* a) {
     off = round_up(off + sizeof(int32_t) * ((size_t)a->n_seqs + 1), 256);
     w.chain_flag = off;
     off = round_up(off + sizeof(int32_t) * (size_t)a->n_seqs * a->n_heads, 256);
+    w.chunk_info = off;
+    off = round_up(off + sizeof(int4) * (size_t)max_chunks_for(a), 256);
     w.records = off;
     off += (size_t)max_chunks_for(a) * a->n_heads * kda::kRecBytes;
     w.total = round_up(off, 256);
@@ -230,6 +232,7 @@ kda_status_t prefill_impl(const kda_prefill_args* a, void* stream, Marks* m) {
     c.a = *a;
     c.chunk_base = reinterpret_cast<int32_t*>(ws + w.chunk_base);
     c.chain_flag = reinterpret_cast<int32_t*>(ws + w.chain_flag);
+    c.chunk_info = reinterpret_cast<int4*>(ws + w.chunk_info);
     c.records = ws + w.records;
     c.max_chunks = max_chunks_for(a);
     c.status = status;

@@ -51,6 +51,7 @@ constexpr float kGuardMin = 7.888609052210118e-31f;   // 2^-100
 struct ChunkLaunch {
     kda_prefill_args a;
     int32_t* chunk_base;   // [n_seqs + 1]: first chunk of each sequence, total at [n_seqs]
+    int4* chunk_info;      // [max_chunks]: {first packed token, tokens (<= 64), sequence, 0}
     int32_t* chain_flag;   // [n_seqs * H]: nonzero = recompute this (sequence, head) token by token
     uint8_t* records;      // [max_chunks * H * kRecBytes]
     int64_t max_chunks;

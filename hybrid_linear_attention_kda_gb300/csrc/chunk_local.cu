@@ -133,21 +133,19 @@ struct Item {
     int n;         // tokens in the chunk
 };
 
-__device__ __forceinline__ Item decode_item(const ChunkLaunch& p, int64_t item) {
+// An item's chunk-table entry (one 16-byte load; the caller issues it early).
+__device__ __forceinline__ int4 item_info(const ChunkLaunch& p, int64_t item, int64_t n_items) {
+    return item < n_items ? p.chunk_info[item / p.a.n_heads] : make_int4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ Item decode_item(const ChunkLaunch& p, int64_t item, int4 info) {
     Item it;
     const int H = p.a.n_heads;
     it.g = item / H;
     it.h = (int)(item % H);
-    int lo = 0, hi = p.a.n_seqs - 1;   // last sequence whose first chunk is <= g
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.chunk_base[mid] <= it.g) lo = mid;
-        else hi = mid - 1;
-    }
-    it.seq = lo;
-    const int64_t tb = p.a.cu_seqlens[lo], te = p.a.cu_seqlens[lo + 1];
-    it.t0 = tb + (it.g - p.chunk_base[lo]) * kC;
-    it.n = (int)(te - it.t0 < kC ? te - it.t0 : kC);
+    it.t0 = info.x;
+    it.n = info.y;
+    it.seq = info.z;
     return it;
 }
 
@@ -176,8 +174,8 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
     }
     // thread 0 issues every copy and MMA and counts them, to drain on a timeout
     uint32_t ld_issued[2] = {0, 0}, ld_waited[2] = {0, 0}, mma_issued = 0, mma_waited = 0;
-    auto issue_load = [&](int64_t item, int st) {
-        const Item it = decode_item(p, item);
+    auto issue_load = [&](int64_t item, int4 info, int st) {
+        const Item it = decode_item(p, item, info);
         uint8_t* S = sm + st * kStageBytes;
         mbar_expect_tx(&ms.bar_load[st], kStageBytes);
         const int32_t x = it.h * kD, y = (int32_t)it.t0;
@@ -188,21 +186,22 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         ld_issued[st] += 1;
     };
     // beta of an item, one token per thread tid < 64
-    auto load_beta = [&](int64_t item) -> float {
+    auto load_beta = [&](int64_t item, int4 info) -> float {
         if (tid >= kC || item >= n_items) return 0.f;
-        const Item it = decode_item(p, item);
+        const Item it = decode_item(p, item, info);
         return tid < it.n ? a.beta[(it.t0 + tid) * H + it.h] : 0.f;
     };
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = ms.tslot;
+    int4 info_cur = item_info(p, first, n_items), info_nxt = item_info(p, first + step, n_items);
     if (tid == 0) {
-        issue_load(first, 0);
-        if (first + step < n_items) issue_load(first + step, 1);
+        issue_load(first, info_cur, 0);
+        if (first + step < n_items) issue_load(first + step, info_nxt, 1);
     }
-    if (tid < kC) ms.beta[0][tid] = load_beta(first);
-    float beta_next = load_beta(first + step);
+    if (tid < kC) ms.beta[0][tid] = load_beta(first, info_cur);
+    float beta_next = load_beta(first + step, info_nxt);
     __syncthreads();
 
     const int c = tid & (kD - 1);
@@ -213,7 +212,8 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
     int k = 0;
     for (int64_t item = first; item < n_items; item += step, ++k) {
         const int st = k & 1;
-        const Item it = decode_item(p, item);
+        const int4 info_nxt2 = item_info(p, item + 2 * step, n_items);   // used at the end of this item
+        const Item it = decode_item(p, item, info_cur);
         const int n = it.n;
         uint8_t* rec = p.records + ((size_t)it.g * H + it.h) * kRecBytes;
         const uint8_t* S = sm + st * kStageBytes;
@@ -480,7 +480,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         }
         fence_after_sync();
         // this stage is no longer read: fetch the item two steps ahead into it
-        if (tid == 0 && item + 2 * step < n_items) issue_load(item + 2 * step, st);
+        if (tid == 0 && item + 2 * step < n_items) issue_load(item + 2 * step, info_nxt2, st);
 
         // ------------------------------------------------------------ phase 4: W and U~ to the record
         {
@@ -503,7 +503,9 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         }
         // beta of the next item into its buffer; start loading the one after
         if (tid < kC) ms.beta[st ^ 1][tid] = beta_next;
-        beta_next = load_beta(item + 2 * step);
+        beta_next = load_beta(item + 2 * step, info_nxt2);
+        info_cur = info_nxt;
+        info_nxt = info_nxt2;
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
@@ -578,6 +580,19 @@ __global__ void __launch_bounds__(1024) chunk_meta_kernel(ChunkLaunch p) {
     if (carry == 0)
         for (int s = tid; s < n; s += blockDim.x) p.chunk_base[s] = 0;
     if (tid == 0) p.chunk_base[n] = (int32_t)carry;
+    __syncthreads();
+    // per-chunk table: first packed token, token count, sequence
+    for (int64_t g = tid; g < carry; g += blockDim.x) {
+        int lo = 0, hi = n - 1;   // last sequence whose first chunk is <= g
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.chunk_base[mid] <= g) lo = mid;
+            else hi = mid - 1;
+        }
+        const int64_t tb = a.cu_seqlens[lo], te = a.cu_seqlens[lo + 1];
+        const int64_t t0 = tb + (g - p.chunk_base[lo]) * kC;
+        p.chunk_info[g] = make_int4((int32_t)t0, (int32_t)(te - t0 < kC ? te - t0 : kC), lo, 0);
+    }
 }
 
 }  // namespace
