@@ -5,7 +5,8 @@
 // The items' q, k, v and alpha tiles ([64 tokens x 128 channels], token rows
 // H*128 elements apart in the packed tensors) arrive by TMA tensor copies into
 // two input stages, so the next item's 80 KiB are in flight while the current
-// item is computed.  Records go straight to the workspace.
+// item is computed.  Record tiles are staged in shared memory and leave by bulk
+// copies.
 //
 // Decay factors are products of alphas over token ranges (no exp / log): with
 // the chunk split into halves of 32 tokens and m the 16th token of a half,
@@ -43,8 +44,10 @@ constexpr uint32_t kAPb = kR + 32768;      // MN-major [c][128 cols r]
 constexpr uint32_t kLbo = 1024, kSbo = 2048;
 constexpr uint32_t kAmat = kR;             // after the A/P MMA: A fp32 [64][64]
 constexpr uint32_t kTf = kR + 16384;       //   T fp32 [64][64]
-constexpr uint32_t kTscr = kR + 32768;     //   block-product scratch, 3 x 16 x 16 fp32
+constexpr uint32_t kTscr = kR + 32768;     //   block-product scratch, 1024 fp32
 constexpr uint32_t kTm = kR + 36864;       //   T^T bf16, MN-major [s][r]
+constexpr uint32_t kPst = kR + 45056;      //   P record tile, staged for its bulk store
+constexpr uint32_t kWst = kR;              // after the W/U~ MMA: W and U~ record tiles, staged
 constexpr uint32_t kMisc = kR + 65536;
 constexpr uint32_t kTmemCols = 128;
 
@@ -77,50 +80,100 @@ __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
 }
 
 // T = (I + A)^-1 for a strictly lower triangular 64 x 64 A (fp32, row-major),
-// by 16 x 16 blocks: the four diagonal blocks by forward substitution, then the
-// off-diagonal blocks one block-diagonal at a time,
-//     T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj .
-// All 256 threads take part; T (including zeros above the diagonal inside the
-// diagonal blocks) goes to Tf, row-major.  Ends with a barrier.
+// by blocks: the four 16 x 16 diagonal blocks by forward substitution, the two
+// 16 x 16 blocks below them inside each 32 x 32 diagonal block, then the lower
+// left 32 x 32 block, each off-diagonal block as
+//     T_ij = -T_ii (A_ij T_jj)       (for the block partition at that level).
+// All 256 threads take part; T (zeros above the diagonal inside the diagonal
+// blocks) goes to Tf, row-major.  scr holds 1024 floats.  Ends with a barrier.
 __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, float* scr, int tid) {
     if (tid < kC) {
         const int o = 16 * (tid >> 4), jj = tid & 15;
         float t[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = r == jj ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) t[r] = r == jj ? 1.f : 0.f;
 #pragma unroll
-            for (int u = 0; u < r; ++u) acc = fmaf(-A[(o + r) * kC + o + u], t[u], acc);
-            t[r] = acc;
+        for (int u = 0; u < 15; ++u) {
+#pragma unroll
+            for (int r = u + 1; r < 16; ++r) t[r] = fmaf(-A[(o + r) * kC + o + u], t[u], t[r]);
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tf[(o + r) * kC + o + jj] = t[r];
+    } else if (tid < 3 * kC) {
+        // blocks (0,1) and (2,3) are zero; the 32 x 32 level reads them
+        const int e = tid - kC, b = e >> 6, x = e & 63;       // 2 blocks x 256 entries, 4 per thread
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int idx = x + 64 * m, rr = idx >> 4, cc = idx & 15;
+            Tf[(32 * b + rr) * kC + 32 * b + 16 + cc] = 0.f;
+        }
     }
     __syncthreads();
+    {   // blocks (1,0) and (3,2): M = A_ij T_jj, then T_ij = -T_ii M
+        const int rr = tid >> 4, cc = tid & 15;
 #pragma unroll
-    for (int dist = 1; dist < 4; ++dist) {
-        const int nblk = 4 - dist;
-        for (int e = tid; e < nblk * 256; e += kThreads) {       // M = sum_k A_ik T_kj
-            const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-            const int i = dist + blk, jb = i - dist;
-            float acc = 0.f;
-            for (int kb = jb; kb < i; ++kb) {
+        for (int m = 0; m < 2; ++m) {
+            const int i = 1 + 2 * m, jb = i - 1;
+            const float* Ar = A + (16 * i + rr) * kC + 16 * jb;
+            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    acc = fmaf(A[(16 * i + rr) * kC + 16 * kb + u], Tf[(16 * kb + u) * kC + 16 * jb + cc], acc);
+            for (int u = 0; u < 16; u += 2) {
+                a0 = fmaf(Ar[u], Tf[(16 * jb + u) * kC + 16 * jb + cc], a0);
+                a1 = fmaf(Ar[u + 1], Tf[(16 * jb + u + 1) * kC + 16 * jb + cc], a1);
             }
-            scr[e] = acc;
+            scr[(m << 8) + tid] = a0 + a1;
         }
         __syncthreads();
-        for (int e = tid; e < nblk * 256; e += kThreads) {       // T_ij = -T_ii M
-            const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-            const int i = dist + blk, jb = i - dist;
-            float acc = 0.f;
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-                acc = fmaf(Tf[(16 * i + rr) * kC + 16 * i + u], scr[(blk << 8) + (u << 4) + cc], acc);
-            Tf[(16 * i + rr) * kC + 16 * jb + cc] = -acc;
+        for (int m = 0; m < 2; ++m) {
+            const int i = 1 + 2 * m, jb = i - 1;
+            const float* Tr = Tf + (16 * i + rr) * kC + 16 * i;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; u += 2) {
+                a0 = fmaf(Tr[u], scr[(m << 8) + (u << 4) + cc], a0);
+                a1 = fmaf(Tr[u + 1], scr[(m << 8) + ((u + 1) << 4) + cc], a1);
+            }
+            Tf[(16 * i + rr) * kC + 16 * jb + cc] = -(a0 + a1);
         }
+        __syncthreads();
+    }
+    {   // lower-left 32 x 32 block: M = A_LL T_00(32), then T_LL = -T_11(32) M
+        const int cc = tid & 31, r0 = tid >> 5;       // rows r0, r0 + 8, r0 + 16, r0 + 24
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < 32; u += 4) {
+            const float t0 = Tf[u * kC + cc], t1 = Tf[(u + 1) * kC + cc];
+            const float t2 = Tf[(u + 2) * kC + cc], t3 = Tf[(u + 3) * kC + cc];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float4 a4 = *reinterpret_cast<const float4*>(A + (32 + r0 + 8 * m) * kC + u);
+                acc[m] = fmaf(a4.x, t0, acc[m]);
+                acc[m] = fmaf(a4.y, t1, acc[m]);
+                acc[m] = fmaf(a4.z, t2, acc[m]);
+                acc[m] = fmaf(a4.w, t3, acc[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) scr[(r0 + 8 * m) * 32 + cc] = acc[m];
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < 4; ++m) acc[m] = 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; u += 4) {
+            const float s0 = scr[u * 32 + cc], s1 = scr[(u + 1) * 32 + cc];
+            const float s2 = scr[(u + 2) * 32 + cc], s3 = scr[(u + 3) * 32 + cc];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float4 t4 = *reinterpret_cast<const float4*>(Tf + (32 + r0 + 8 * m) * kC + 32 + u);
+                acc[m] = fmaf(t4.x, s0, acc[m]);
+                acc[m] = fmaf(t4.y, s1, acc[m]);
+                acc[m] = fmaf(t4.z, s2, acc[m]);
+                acc[m] = fmaf(t4.w, s3, acc[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) Tf[(32 + r0 + 8 * m) * kC + cc] = -acc[m];
         __syncthreads();
     }
 }
@@ -195,6 +248,12 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = ms.tslot;
+    if (tid == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm.q)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm.k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm.v)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm.alpha)) : "memory");
+    }
     int4 info_cur = item_info(p, first, n_items), info_nxt = item_info(p, first + step, n_items);
     if (tid == 0) {
         issue_load(first, info_cur, 0);
@@ -255,6 +314,12 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         }
         const float H0 = hh ? oth : own, H1 = hh ? own : oth;
         if (hh == 1) reinterpret_cast<float*>(rec + kRecG)[c] = H0 * H1;
+        // the alpha tile is consumed (it now stages Q~ and Kbar); the previous
+        // item's staged W / U~ must have left shared memory before the A/P
+        // operands overwrite it
+        if (tid == 0) bulk_wait_read();
+        __syncthreads();
+        const uint32_t qk_stage = Ss + kSal;      // Q~ tile, then Kbar tile
 
         bool guard_bad = false;
         {   // forward: Gamma (Q~ to the record)
@@ -265,7 +330,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
                 const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
                 P *= al[i];
                 gq[i & 7] = qf * (hh ? H0 * P : P);
-                if ((i & 7) == 7) stg16(rec + kRecQ + row64_chunk_off(c, (32 * hh + (i & ~7)) >> 3), pack8(gq));
+                if ((i & 7) == 7) sts16(qk_stage + row64_chunk_off(c, (32 * hh + (i & ~7)) >> 3), pack8(gq));
             }
         }
         {   // forward from the half's reference token: phi = E, psi = 1/E (local tokens 16..31)
@@ -298,7 +363,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
                 kb[i & 7] = kf * (hh ? Q : Q * H1);
                 kx[i & 7] = kf * (Q * mid);
                 if ((i & 7) == 0) {
-                    stg16(rec + kRecK + row64_chunk_off(c, (32 * hh + i) >> 3), pack8(kb));
+                    sts16(qk_stage + 16384 + row64_chunk_off(c, (32 * hh + i) >> 3), pack8(kb));
                     if (!hh) sts16(apa + mn_chunk(64 + i, c), pack8(kx));
                 }
                 Q *= al[i];
@@ -332,6 +397,8 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         fence_after_sync();
 
         if (tid == 0) {
+            bulk_s2g(rec + kRecQ, S + kSal, 32768);     // Q~ and Kbar are adjacent in the record
+            bulk_commit();
             if (ms.guard_fail) {
                 atomicOr(&p.chain_flag[(int64_t)it.seq * H + it.h], 1);
                 ms.guard_fail = 0;
@@ -368,12 +435,12 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         x[e] = (warp == 2 || r0 + e >= s) ? __uint_as_float(v[8 * e8 + e]) : 0.f;
-                    stg16(rec + kRecP + row64_chunk_off(s, r0 >> 3), pack8(x));
+                    sts16(s_base + kPst + row64_chunk_off(s, r0 >> 3), pack8(x));
                 }
             }
             if (warp == 1) {
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) stg16(rec + kRecP + row64_chunk_off(s, cc), make_uint4(0u, 0u, 0u, 0u));
+                for (int cc = 0; cc < 4; ++cc) sts16(s_base + kPst + row64_chunk_off(s, cc), make_uint4(0u, 0u, 0u, 0u));
             }
         } else if (warp >= 4 && warp < 7) {
             const int wq = warp - 4;
@@ -395,9 +462,14 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
                 for (int r = 0; r < 32; ++r) Am[r * kC + s] = 0.f;
             }
         }
+        fence_async_smem();
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
+        if (tid == 0) {
+            bulk_s2g(rec + kRecP, sm + kPst, 8192);
+            bulk_commit();
+        }
 
         // ------------------------------------------------------------ phase 3: X^T, Y^T, T
         uint32_t vq[16];
@@ -480,13 +552,16 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         }
         fence_after_sync();
         // this stage is no longer read: fetch the item two steps ahead into it
-        if (tid == 0 && item + 2 * step < n_items) issue_load(item + 2 * step, info_nxt2, st);
+        if (tid == 0 && item + 2 * step < n_items) {
+            bulk_wait_read();                          // the staged Q~ / Kbar left this stage
+            issue_load(item + 2 * step, info_nxt2, st);
+        }
 
         // ------------------------------------------------------------ phase 4: W and U~ to the record
         {
             const int row = 32 * (warp & 3) + lane;
             const uint32_t col0 = warp < 4 ? 0u : 64u;
-            uint8_t* dst = rec + (warp < 4 ? kRecW : kRecU);
+            const uint32_t dst = s_base + kWst + (warp < 4 ? 0u : 16384u);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t v[16];
@@ -497,7 +572,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * e8 + e]);
-                    stg16(dst + row64_chunk_off(row, 2 * q4 + e8), pack8(x));
+                    sts16(dst + row64_chunk_off(row, 2 * q4 + e8), pack8(x));
                 }
             }
         }
@@ -506,11 +581,18 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         beta_next = load_beta(item + 2 * step, info_nxt2);
         info_cur = info_nxt;
         info_nxt = info_nxt2;
+        fence_async_smem();
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
+        if (tid == 0) {
+            bulk_s2g(rec + kRecW, sm + kWst, 16384);
+            bulk_s2g(rec + kRecU, sm + kWst + 16384, 16384);
+            bulk_commit();
+        }
     }
 
+    if (tid == 0) bulk_wait_all();                     // staged records written out
     if (!ok && tid == 0) {
         // let this CTA's own copies and MMAs in flight land (bounded) before
         // shared and tensor memory are released

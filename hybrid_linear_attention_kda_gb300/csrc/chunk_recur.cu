@@ -28,7 +28,7 @@ constexpr uint32_t kStageStride = 74752;  // kRecBytes rounded up to 1024
 constexpr uint32_t kMisc = kStage0 + 2 * kStageStride;
 constexpr size_t kSmemBytes = kMisc + 64 + 1024;
 
-constexpr uint32_t kTmemCols = 512;       // D1 [0,64), D2 x2 [64,192), D3 [256,384)
+constexpr uint32_t kTmemCols = 512;       // [D1 | D2] x 2 at [0,128) and [128,256), D3 [256,384)
 
 struct Misc {
     uint64_t bar_load[2];
@@ -99,8 +99,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     __syncthreads();
     fence_after_sync();
     const uint32_t tbase = ms.tslot;
-    const uint32_t tD1 = tbase, tD3 = tbase + 256;
-    auto tD2 = [&](int64_t lc) -> uint32_t { return tbase + 64 + 64 * (uint32_t)(lc & 1); };
+    const uint32_t tD3 = tbase + 256;
+    // [D1 | D2] of chunk lc: one N = 128 accumulator, double-buffered
+    auto tD1 = [&](int64_t lc) -> uint32_t { return tbase + 128 * (uint32_t)(lc & 1); };
+    auto tD2 = [&](int64_t lc) -> uint32_t { return tbase + 128 * (uint32_t)(lc & 1) + 64; };
 
     // Thread 0 issues every copy and MMA and keeps the counts needed to drain
     // them if a wait ever times out.
@@ -117,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         ld_issued[st] += 1;
     };
     const uint32_t id64 = idesc_bf16(128, 64, false, true);
+    const uint32_t id128mn = idesc_bf16(128, 128, false, true);
     const uint32_t id128 = idesc_bf16(128, 128, false, false);
     // Descriptors are built once; a k-step only moves the start address, which
     // is the low 14-bit field (address >> 4; every operand here lies below
@@ -124,25 +127,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     const uint64_t dSa = sdesc(s_base + kSa, 16, 1024);
     const uint64_t dUa = sdesc(s_base + kUa, 16, 1024);
     const uint64_t dMN = sdesc(0, 1024, 1024);       // MN-major record tile, start added per use
+    // W and Q~ tiles are adjacent in the record (16 KiB apart): one MN-major
+    // operand of N = 128 whose two 64-wide blocks are 16 KiB apart
+    static_assert(kRecQ == kRecW + 16384, "record layout");
+    const uint64_t dWQ = sdesc(0, 16384, 1024);
     const uint64_t dKM = sdesc(0, 16, 1024);         // K-major record tile
     auto at = [](uint64_t desc, uint32_t byte_off) -> uint64_t { return desc + (uint64_t)(byte_off >> 4); };
-    // (a) D1 = S^T W^T (own commit: the U epilogue waits only for it) and
-    // (b) D2 = S^T Q~^T for chunk lc
+    // (a) D1 = S^T W^T and (b) D2 = S^T Q~^T for chunk lc, as one N = 128 MMA chain
     auto issue_ab = [&](int64_t lc) {
         const uint32_t stage = stage_addr(lc);
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks)
-            mma_bf16(tD1, at(dSa, (ks >> 2) * 16384 + (ks & 3) * 32), at(dMN, stage + kRecW + ks * 2048), id64,
-                     ks > 0 ? 1u : 0u);
+            mma_bf16(tD1(lc), at(dSa, (ks >> 2) * 16384 + (ks & 3) * 32), at(dWQ, stage + kRecW + ks * 2048),
+                     id128mn, ks > 0 ? 1u : 0u);
         mma_commit(&ms.bar_a);
         a_issued += 1;
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks)
-            mma_bf16(tD2(lc), at(dSa, (ks >> 2) * 16384 + (ks & 3) * 32), at(dMN, stage + kRecQ + ks * 2048), id64,
-                     ks > 0 ? 1u : 0u);
     };
-    // (c) D2 += U^T P^T and (d) D3 = U^T Kbar for chunk lc; the commit also
-    // covers (b)
+    // (c) D2 += U^T P^T and (d) D3 = U^T Kbar for chunk lc
     auto issue_cd = [&](int64_t lc) {
         const uint32_t stage = stage_addr(lc);
 #pragma unroll
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         // (a) epilogue: U^T = U~^T - D1 for this thread's 16 tokens
         {
             uint32_t v[16];
-            tmem_ld16(tD1 + lanebase + tq, v);
+            tmem_ld16(tD1(lc) + lanebase + tq, v);
             tmem_wait_ld();
 #pragma unroll
             for (int e8 = 0; e8 < 2; ++e8) {
