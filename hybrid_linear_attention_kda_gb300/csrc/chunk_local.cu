@@ -6,7 +6,7 @@
 // H*128 elements apart in the packed tensors) arrive by TMA tensor copies into
 // two input stages, so the next item's 80 KiB are in flight while the current
 // item is computed.  Record tiles are staged in shared memory and leave by bulk
-// copies.
+// copies; X^T and Y^T are built in place of the q and v tiles once those are read.
 //
 // Decay factors are products of alphas over token ranges (no exp / log): with
 // the chunk split into halves of 32 tokens and m the 16th token of a half,
@@ -72,7 +72,6 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
                       pack_bf16(v[6], v[7]));
 }
 __device__ __forceinline__ void sts16(uint32_t saddr, uint4 v) { st_shared_v4(saddr, v.x, v.y, v.z, v.w); }
-__device__ __forceinline__ void stg16(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 // byte offset of the 16-byte chunk (mn .. mn+7, k) of an MN-major tile
 __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
@@ -290,8 +289,9 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         const float* sal = reinterpret_cast<const float*>(S + kSal);
         const uint16_t* sq = reinterpret_cast<const uint16_t*>(S + kSq);
         const uint16_t* sk = reinterpret_cast<const uint16_t*>(S + kSk);
+        const uint16_t* sv = reinterpret_cast<const uint16_t*>(S + kSv);
         float al[32];
-        uint32_t qp[16], kp[16];
+        uint32_t qp[16], kp[16], vq[16];
         float own = 1.f;
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
@@ -301,6 +301,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             al[i + 1] = v1 ? sal[(r + 1) * kD + c] : 1.f;
             qp[i >> 1] = (v0 ? (uint32_t)sq[r * kD + c] : 0u) | ((v1 ? (uint32_t)sq[(r + 1) * kD + c] : 0u) << 16);
             kp[i >> 1] = (v0 ? (uint32_t)sk[r * kD + c] : 0u) | ((v1 ? (uint32_t)sk[(r + 1) * kD + c] : 0u) << 16);
+            vq[i >> 1] = (v0 ? (uint32_t)sv[r * kD + c] : 0u) | ((v1 ? (uint32_t)sv[(r + 1) * kD + c] : 0u) << 16);
             own *= al[i];
             own *= al[i + 1];
         }
@@ -314,23 +315,34 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         }
         const float H0 = hh ? oth : own, H1 = hh ? own : oth;
         if (hh == 1) reinterpret_cast<float*>(rec + kRecG)[c] = H0 * H1;
-        // the alpha tile is consumed (it now stages Q~ and Kbar); the previous
-        // item's staged W / U~ must have left shared memory before the A/P
-        // operands overwrite it
+        // the q, v and alpha tiles are consumed (they now hold X^T, Y^T and the
+        // staged Q~ / Kbar); the previous item's staged W / U~ must have left
+        // shared memory before the A/P operands overwrite it
         if (tid == 0) bulk_wait_read();
         __syncthreads();
         const uint32_t qk_stage = Ss + kSal;      // Q~ tile, then Kbar tile
 
         bool guard_bad = false;
-        {   // forward: Gamma (Q~ to the record)
+        {   // forward: Gamma -> Q~ (record) and X^T = beta Gamma k (q tile); Y^T = beta v (v tile)
             float P = 1.f;
-            float gq[8];
+            float gq[8], xk[8], yv[8];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
+                const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+                const float vf = (i & 1) ? bf_hi(vq[i >> 1]) : bf_lo(vq[i >> 1]);
+                const float b = bsm[32 * hh + i];
                 P *= al[i];
-                gq[i & 7] = qf * (hh ? H0 * P : P);
-                if ((i & 7) == 7) sts16(qk_stage + row64_chunk_off(c, (32 * hh + (i & ~7)) >> 3), pack8(gq));
+                const float G = hh ? H0 * P : P;
+                gq[i & 7] = qf * G;
+                xk[i & 7] = b * kf * G;
+                yv[i & 7] = b * vf;
+                if ((i & 7) == 7) {
+                    const uint32_t cc = (32 * hh + (i & ~7)) >> 3;
+                    sts16(qk_stage + row64_chunk_off(c, cc), pack8(gq));
+                    sts16(Ss + kSq + row64_chunk_off(c, cc), pack8(xk));
+                    sts16(Ss + kSv + row64_chunk_off(c, cc), pack8(yv));
+                }
             }
         }
         {   // forward from the half's reference token: phi = E, psi = 1/E (local tokens 16..31)
@@ -471,44 +483,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             bulk_commit();
         }
 
-        // ------------------------------------------------------------ phase 3: X^T, Y^T, T
-        uint32_t vq[16];
-        {
-            const uint16_t* sv = reinterpret_cast<const uint16_t*>(S + kSv);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const int r = 32 * hh + i;
-                vq[i >> 1] = (r < n ? (uint32_t)sv[r * kD + c] : 0u) | ((r + 1 < n ? (uint32_t)sv[(r + 1) * kD + c] : 0u) << 16);
-            }
-            // X^T row c (beta_r Gamma_rc k_rc) into the stage's q tile, which is no longer read
-            float Gm = hh ? H0 : 1.f;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * cc + e;
-                    Gm *= al[i];
-                    const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-                    x[e] = bsm[32 * hh + i] * kf * Gm;
-                }
-                sts16(Ss + kSq + row64_chunk_off(c, 4 * hh + cc), pack8(x));
-            }
-        }
-        __syncthreads();   // every thread holds its v column: the v tile can be overwritten
-        {   // Y^T row c (beta_r v_rc) into the stage's v tile
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                float y[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * cc + e;
-                    const float vf = (i & 1) ? bf_hi(vq[i >> 1]) : bf_lo(vq[i >> 1]);
-                    y[e] = bsm[32 * hh + i] * vf;
-                }
-                sts16(Ss + kSv + row64_chunk_off(c, 4 * hh + cc), pack8(y));
-            }
-        }
+        // ------------------------------------------------------------ phase 3: T
         invert_unit_lower(reinterpret_cast<const float*>(sm + kAmat), reinterpret_cast<float*>(sm + kTf),
                           reinterpret_cast<float*>(sm + kTscr), tid);
         {   // T^T row s (= column s of T, zero above the diagonal) as the MN-major [s][r] operand

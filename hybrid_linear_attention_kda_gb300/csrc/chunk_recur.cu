@@ -3,38 +3,48 @@
 //
 // Everything runs transposed so that the value channel j (128 of them) is the
 // MMA M dimension and the TMEM lane.  Per chunk, with S^T [j][c] the state:
-//   (a) D1 = S^T W^T             U^T = U~^T - D1            (bf16 U^T to smem)
-//   (b) D2 = S^T Q~^T
-//   (c) D2 += U^T P^T            O^T = D2
-//   (d) D3 = U^T Kbar            S^T <- S^T Diag(gamma) + D3  (fp32, registers)
-// Thread (j, quarter) keeps 32 fp32 state entries S[c][j] for its quarter of the
-// key channels c; the bf16 copy of S^T in shared memory is the A operand of (a) and
-// (b).  The chunk records written by stage one arrive with bulk copies, two
-// chunks in flight.  The output accumulator is double-buffered so that the
-// outputs of one chunk are stored while the next chunk's MMAs run.  A snapshot is written after every chunk that ends at an
-// absolute position that is a multiple of snap_interval ("Kimi K3 Tech Intro",
-// sections 2.2-2.4), straight from the fp32 registers.
+//   (ab) [D1 | D2] = S^T [W^T | Q~^T]        one N = 128 MMA chain
+//   (d)  D3  = U^T Kbar                       U^T = U~^T - D1 (bf16, smem)
+//   (c)  D2 += U^T P^T                        O^T = D2
+//   then S^T <- S^T Diag(gamma) + D3          fp32, registers
+// The chain that carries the state is (ab) -> U -> (d) -> S -> next (ab); (c)
+// and the outputs run beside it.  The CTA is split by role:
+//   warps 0-7   state group: thread (j, half) keeps 64 fp32 entries S[c][j] for
+//               its half of the key channels, builds U^T and the bf16 copy of
+//               S^T (the A operand of (ab)), writes snapshots
+//               ("Kimi K3 Tech Intro", sections 2.2-2.4) and the final state;
+//   warps 8-11  output group: O^T from TMEM to the packed output;
+//   warp 12     one thread issues the record copies (two chunks in flight) and
+//               every MMA, in dependency order, through mbarriers.
+// [D1 | D2] is double-buffered in TMEM so the outputs of one chunk are read while
+// the next chunk's MMAs run.
 #include "chunk_common.cuh"
 
 namespace kda {
 namespace {
 using namespace tc;
 
-constexpr int kThreads = 512;      // 16 warps: 4 lane quarters x 4 key-channel quarters
+constexpr int kStateWarps = 8, kOutWarps = 4;
+constexpr int kThreads = 32 * (kStateWarps + kOutWarps + 1);
+constexpr int kIssuerWarp = kStateWarps + kOutWarps;
 constexpr uint32_t kSa = 0;               // S^T bf16, K-major [j][c], two 64-wide regions
 constexpr uint32_t kUa = 32768;           // U^T bf16, K-major [j][t]
 constexpr uint32_t kStage0 = 49152;
 constexpr uint32_t kStageStride = 74752;  // kRecBytes rounded up to 1024
 constexpr uint32_t kMisc = kStage0 + 2 * kStageStride;
-constexpr size_t kSmemBytes = kMisc + 64 + 1024;
-
+constexpr size_t kSmemBytes = kMisc + 128 + 1024;
 constexpr uint32_t kTmemCols = 512;       // [D1 | D2] x 2 at [0,128) and [128,256), D3 [256,384)
 
 struct Misc {
-    uint64_t bar_load[2];
-    uint64_t bar_a;
-    uint64_t bar_cd;
+    uint64_t bar_load[2];   // record copies (tx bytes)
+    uint64_t bar_ab;        // MMA commit after (ab)
+    uint64_t bar_d;         // MMA commit after (d)
+    uint64_t bar_c;         // MMA commit after (c)
+    uint64_t bar_u;         // state group: U^T written            (256 arrivals)
+    uint64_t bar_s;         // state group: bf16 S^T written        (256 arrivals)
+    uint64_t bar_o;         // output group: D2 read from TMEM     (128 arrivals)
     uint32_t tslot;
+    int32_t failed;
 };
 
 __device__ __forceinline__ void sts16(uint32_t saddr, uint4 v) { st_shared_v4(saddr, v.x, v.y, v.z, v.w); }
@@ -58,43 +68,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     const int64_t g0 = p.chunk_base[seq];
     const int64_t nc = p.chunk_base[seq + 1] - g0;
     if (nc < 0 || g0 + nc > p.max_chunks) return;
-
-    const int jq = warp & 3, ch = warp >> 2;
-    const int j = 32 * jq + lane;          // value channel (TMEM lane)
-    const int cbase = 32 * ch;             // this thread's 32 key channels
-    const int tq = 16 * ch;                // and its 16 tokens in the per-token epilogues
-    const uint32_t lanebase = (uint32_t)(32 * jq) << 16;
     const int64_t slot_stride = (int64_t)H * kD * kD;
     const int64_t head_off = (int64_t)h * kD * kD;
-
-    float S[32];
-    if (init >= 0) {
-        const float* S0 = a.pool + (int64_t)init * slot_stride + head_off;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) S[i] = S0[(int64_t)(cbase + i) * kD + j];
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) S[i] = 0.f;
-    }
-    auto write_sa = [&]() {
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const uint4 v = make_uint4(pack_bf16(S[8 * m], S[8 * m + 1]), pack_bf16(S[8 * m + 2], S[8 * m + 3]),
-                                       pack_bf16(S[8 * m + 4], S[8 * m + 5]), pack_bf16(S[8 * m + 6], S[8 * m + 7]));
-            sts16(s_base + kSa + kmajor_off(j, cbase + 8 * m, kD), v);
-        }
-    };
-    write_sa();
 
     if (warp == 0) tmem_alloc(&ms.tslot, kTmemCols);
     if (tid == 0) {
         mbar_init(&ms.bar_load[0], 1);
         mbar_init(&ms.bar_load[1], 1);
-        mbar_init(&ms.bar_a, 1);
-        mbar_init(&ms.bar_cd, 1);
+        mbar_init(&ms.bar_ab, 1);
+        mbar_init(&ms.bar_d, 1);
+        mbar_init(&ms.bar_c, 1);
+        mbar_init(&ms.bar_u, 32 * kStateWarps);
+        mbar_init(&ms.bar_s, 32 * kStateWarps);
+        mbar_init(&ms.bar_o, 32 * kOutWarps);
+        ms.failed = 0;
         fence_mbar_init();
     }
-    fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -103,201 +92,225 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     // [D1 | D2] of chunk lc: one N = 128 accumulator, double-buffered
     auto tD1 = [&](int64_t lc) -> uint32_t { return tbase + 128 * (uint32_t)(lc & 1); };
     auto tD2 = [&](int64_t lc) -> uint32_t { return tbase + 128 * (uint32_t)(lc & 1) + 64; };
-
-    // Thread 0 issues every copy and MMA and keeps the counts needed to drain
-    // them if a wait ever times out.
-    uint32_t ld_issued[2] = {0, 0}, ld_waited[2] = {0, 0};
-    uint32_t a_issued = 0, a_waited = 0, cd_issued = 0, cd_waited = 0;
-    auto rec_ptr = [&](int64_t lc) -> const uint8_t* {
-        return p.records + ((size_t)(g0 + lc) * H + h) * kRecBytes;
-    };
-    auto stage_addr = [&](int64_t lc) -> uint32_t { return s_base + kStage0 + (uint32_t)(lc & 1) * kStageStride; };
-    auto issue_load = [&](int64_t lc) {
-        const int st = (int)(lc & 1);
-        mbar_expect_tx(&ms.bar_load[st], kRecBytes);
-        bulk_g2s(sm + kStage0 + st * kStageStride, rec_ptr(lc), kRecBytes, &ms.bar_load[st]);
-        ld_issued[st] += 1;
-    };
-    const uint32_t id64 = idesc_bf16(128, 64, false, true);
-    const uint32_t id128mn = idesc_bf16(128, 128, false, true);
-    const uint32_t id128 = idesc_bf16(128, 128, false, false);
-    // Descriptors are built once; a k-step only moves the start address, which
-    // is the low 14-bit field (address >> 4; every operand here lies below
-    // 256 KiB, so adding the step never carries out of the field).
-    const uint64_t dSa = sdesc(s_base + kSa, 16, 1024);
-    const uint64_t dUa = sdesc(s_base + kUa, 16, 1024);
-    const uint64_t dMN = sdesc(0, 1024, 1024);       // MN-major record tile, start added per use
-    // W and Q~ tiles are adjacent in the record (16 KiB apart): one MN-major
-    // operand of N = 128 whose two 64-wide blocks are 16 KiB apart
-    static_assert(kRecQ == kRecW + 16384, "record layout");
-    const uint64_t dWQ = sdesc(0, 16384, 1024);
-    const uint64_t dKM = sdesc(0, 16, 1024);         // K-major record tile
-    auto at = [](uint64_t desc, uint32_t byte_off) -> uint64_t { return desc + (uint64_t)(byte_off >> 4); };
-    // (a) D1 = S^T W^T and (b) D2 = S^T Q~^T for chunk lc, as one N = 128 MMA chain
-    auto issue_ab = [&](int64_t lc) {
-        const uint32_t stage = stage_addr(lc);
-#pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks)
-            mma_bf16(tD1(lc), at(dSa, (ks >> 2) * 16384 + (ks & 3) * 32), at(dWQ, stage + kRecW + ks * 2048),
-                     id128mn, ks > 0 ? 1u : 0u);
-        mma_commit(&ms.bar_a);
-        a_issued += 1;
-    };
-    // (c) D2 += U^T P^T and (d) D3 = U^T Kbar for chunk lc
-    auto issue_cd = [&](int64_t lc) {
-        const uint32_t stage = stage_addr(lc);
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tD2(lc), at(dUa, ks * 32), at(dMN, stage + kRecP + ks * 2048), id64, 1u);
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tD3, at(dUa, ks * 32), at(dKM, stage + kRecK + ks * 32), id128, ks > 0 ? 1u : 0u);
-        mma_commit(&ms.bar_cd);
-        cd_issued += 1;
-    };
-    __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
-    // outputs of chunk lc (its O^T is complete in D2(lc)): this thread's 16 tokens
-    auto store_outputs = [&](int64_t lc) {
-        const int64_t t0 = tb + lc * kC;
-        const int n = (int)(te - t0 < kC ? te - t0 : kC);
-        uint32_t v[16];
-        tmem_ld16(tD2(lc) + lanebase + tq, v);
-        tmem_wait_ld();
-        __nv_bfloat16* orow = og + ((t0 + tq) * H + h) * kD + j;
-        const int64_t ostride = (int64_t)H * kD;
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-            if (tq + e < n) orow[e * ostride] = __float2bfloat16_rn(a.scale * __uint_as_float(v[e]));
+    auto stage_of = [&](int64_t lc) -> uint32_t { return kStage0 + (uint32_t)(lc & 1) * kStageStride; };
+    // a bounded wait; a timeout marks the CTA failed (every role then stops)
+    auto waitb = [&](uint64_t* bar, uint32_t parity) -> bool {
+        if (mbar_wait(bar, parity)) return true;
+        atomicExch(&ms.failed, 1);
+        return false;
     };
 
-    bool ok = true;
-    if (tid == 0 && nc > 0) {
-        issue_load(0);
-        if (nc > 1) issue_load(1);
-        ok = mbar_wait(&ms.bar_load[0], 0);
-        if (ok) {
-            ld_waited[0] = 1;
-            issue_ab(0);
-        }
-    }
-    ok = !__syncthreads_or(!ok);
-    for (int64_t lc = 0; lc < nc && ok; ++lc) {
-        const int st = (int)(lc & 1);
-        const uint8_t* stage_p = sm + kStage0 + st * kStageStride;
-        const uint32_t par = (uint32_t)(lc & 1);
-        // the record of chunk lc has landed (thread 0 saw it before issuing (a))
-        ok = mbar_wait(&ms.bar_load[st], (uint32_t)((lc >> 1) & 1)) && mbar_wait(&ms.bar_a, par);
-        if (tid == 0 && ok) a_waited += 1;
-        if (__syncthreads_or(!ok)) {
-            ok = false;
-            break;
-        }
-        fence_after_sync();
-
-        // (a) epilogue: U^T = U~^T - D1 for this thread's 16 tokens
-        {
-            uint32_t v[16];
-            tmem_ld16(tD1(lc) + lanebase + tq, v);
-            tmem_wait_ld();
+    if (warp == kIssuerWarp) {
+        // ------------------------------------------------------------------ issuer
+        if (lane == 0) {
+            uint32_t ld_issued[2] = {0, 0}, ld_waited[2] = {0, 0};
+            uint32_t n_c = 0, w_c = 0;      // commits after (c) issued / waited by this thread
+            const uint32_t id128mn = idesc_bf16(128, 128, false, true);
+            const uint32_t id64 = idesc_bf16(128, 64, false, true);
+            const uint32_t id128 = idesc_bf16(128, 128, false, false);
+            // Descriptors are built once; a k-step only moves the start address,
+            // the low 14-bit field (address >> 4; all operands lie below 256 KiB,
+            // so adding a step never carries out of the field).
+            const uint64_t dSa = sdesc(s_base + kSa, 16, 1024);
+            const uint64_t dUa = sdesc(s_base + kUa, 16, 1024);
+            const uint64_t dMN = sdesc(0, 1024, 1024);
+            const uint64_t dKM = sdesc(0, 16, 1024);
+            // W and Q~ tiles are adjacent in the record (16 KiB apart): one
+            // MN-major operand of N = 128 whose two 64-wide blocks are 16 KiB apart
+            static_assert(kRecQ == kRecW + 16384, "record layout");
+            const uint64_t dWQ = sdesc(0, 16384, 1024);
+            auto at = [](uint64_t desc, uint32_t byte_off) -> uint64_t { return desc + (uint64_t)(byte_off >> 4); };
+            auto load = [&](int64_t lc) {
+                const int st = (int)(lc & 1);
+                mbar_expect_tx(&ms.bar_load[st], kRecBytes);
+                bulk_g2s(sm + stage_of(lc), p.records + ((size_t)(g0 + lc) * H + h) * kRecBytes, kRecBytes,
+                         &ms.bar_load[st]);
+                ld_issued[st] += 1;
+            };
+            auto wait_load = [&](int64_t lc) -> bool {
+                const int st = (int)(lc & 1);
+                if (!waitb(&ms.bar_load[st], (uint32_t)((lc >> 1) & 1))) return false;
+                ld_waited[st] += 1;
+                return true;
+            };
+            auto issue_ab = [&](int64_t lc) {
+                const uint32_t stage = s_base + stage_of(lc);
 #pragma unroll
-            for (int e8 = 0; e8 < 2; ++e8) {
-                const int cc = 2 * ch + e8;
-                const uint4 ut = *reinterpret_cast<const uint4*>(stage_p + kRecU + row64_chunk_off(j, cc));
-                const uint32_t uw[4] = {ut.x, ut.y, ut.z, ut.w};
-                uint32_t outw[4];
+                for (int ks = 0; ks < kD / 16; ++ks)
+                    mma_bf16(tD1(lc), at(dSa, (ks >> 2) * 16384 + (ks & 3) * 32), at(dWQ, stage + kRecW + ks * 2048),
+                             id128mn, ks > 0 ? 1u : 0u);
+                mma_commit(&ms.bar_ab);
+            };
+            auto issue_dc = [&](int64_t lc) {
+                const uint32_t stage = s_base + stage_of(lc);
 #pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    const float u0 = __uint_as_float(uw[e2] << 16) - __uint_as_float(v[8 * e8 + 2 * e2]);
-                    const float u1 = __uint_as_float(uw[e2] & 0xFFFF0000u) - __uint_as_float(v[8 * e8 + 2 * e2 + 1]);
-                    outw[e2] = pack_bf16(u0, u1);
-                }
-                st_shared_v4(s_base + kUa + row64_chunk_off(j, cc), outw[0], outw[1], outw[2], outw[3]);
+                for (int ks = 0; ks < kC / 16; ++ks)
+                    mma_bf16(tD3, at(dUa, ks * 32), at(dKM, stage + kRecK + ks * 32), id128, ks > 0 ? 1u : 0u);
+                mma_commit(&ms.bar_d);
+#pragma unroll
+                for (int ks = 0; ks < kC / 16; ++ks)
+                    mma_bf16(tD2(lc), at(dUa, ks * 32), at(dMN, stage + kRecP + ks * 2048), id64, 1u);
+                mma_commit(&ms.bar_c);
+                n_c += 1;
+            };
+            bool ok = true;
+            if (nc > 0) {
+                load(0);
+                if (nc > 1) load(1);
+                ok = waitb(&ms.bar_s, 0) && wait_load(0);           // initial bf16 state and record 0
+                if (ok) issue_ab(0);
             }
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
-        if (tid == 0) issue_cd(lc);
-
-        // outputs of the previous chunk while (c) and (d) run
-        if (lc > 0) store_outputs(lc - 1);
-
-        ok = mbar_wait(&ms.bar_cd, par);
-        if (tid == 0 && ok) cd_waited += 1;
-        if (__syncthreads_or(!ok)) {
-            ok = false;
-            break;
-        }
-        fence_after_sync();
-
-        // (d) epilogue: S <- gamma * S + D3 ; bf16 copy for the next chunk
-        const float* gam = reinterpret_cast<const float*>(stage_p + kRecG) + cbase;
-#pragma unroll
-        for (int q4 = 0; q4 < 2; ++q4) {
-            uint32_t v[16];
-            tmem_ld16(tD3 + lanebase + cbase + 16 * q4, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) S[16 * q4 + e] = fmaf(gam[16 * q4 + e], S[16 * q4 + e], __uint_as_float(v[e]));
-        }
-        write_sa();
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
-
-        // stage st is free again: refill it two chunks ahead; start the next chunk
-        if (tid == 0) {
-            if (lc + 2 < nc) issue_load(lc + 2);
-            if (lc + 1 < nc) {
-                const int st1 = st ^ 1;
-                if (mbar_wait(&ms.bar_load[st1], (uint32_t)(((lc + 1) >> 1) & 1))) {
-                    ld_waited[st1] += 1;
+            for (int64_t lc = 0; lc < nc && ok; ++lc) {
+                const uint32_t par = (uint32_t)(lc & 1);
+                if (!(ok = waitb(&ms.bar_u, par))) break;          // U^T of lc written
+                fence_after_sync();
+                issue_dc(lc);
+                if (!(ok = waitb(&ms.bar_s, par ^ 1))) break;      // state after lc written
+                if (!(ok = waitb(&ms.bar_c, par))) break;          // every MMA of lc done
+                w_c += 1;
+                fence_after_sync();
+                if (lc + 2 < nc) load(lc + 2);                      // record stage of lc is free
+                if (lc + 1 < nc) {
+                    if (!(ok = wait_load(lc + 1))) break;
+                    if (lc >= 1 && !(ok = waitb(&ms.bar_o, (uint32_t)((lc - 1) & 1)))) break;   // D2 buffer free
                     issue_ab(lc + 1);
                 }
             }
+            if (!ok) {
+                // let this CTA's own copies and MMAs land (bounded) before
+                // shared and tensor memory are released
+                for (int st = 0; st < 2; ++st)
+                    for (uint32_t l = ld_waited[st]; l < ld_issued[st]; ++l) mbar_wait(&ms.bar_load[st], l & 1);
+                for (uint32_t m = w_c; m < n_c; ++m) mbar_wait(&ms.bar_c, m & 1);
+            }
         }
-
-        // snapshot after this chunk, straight from the fp32 registers
-        const int64_t t0 = tb + lc * kC;
-        const int n = (int)(te - t0 < kC ? te - t0 : kC);
-        const int64_t p_end = pos0 + lc * kC + n;
-        if (a.snap_table && p_end % a.snap_interval == 0) {
-            const int64_t ord = p_end / a.snap_interval - 1;
-            if (ord >= a.snap_table_stride) {
-                if (tid == 0) flag(p.status, KDA_DEV_BAD_ORDINAL);
-            } else {
-                const int32_t slot = a.snap_table[(int64_t)seq * a.snap_table_stride + ord];
-                if (slot >= 0 && (int64_t)slot < a.n_slots) {
-                    float* dst = a.pool + (int64_t)slot * slot_stride + head_off;
+    } else if (warp < kStateWarps) {
+        // ------------------------------------------------------------------ state group
+        const int jq = warp & 3, ch = warp >> 2;
+        const int j = 32 * jq + lane;          // value channel (TMEM lane)
+        const int cbase = 64 * ch;             // this thread's 64 key channels
+        const int tq = 32 * ch;                // and its 32 tokens in the U epilogue
+        const uint32_t lanebase = (uint32_t)(32 * jq) << 16;
+        float S[64];
+        if (init >= 0) {
+            const float* S0 = a.pool + (int64_t)init * slot_stride + head_off;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
-                } else if (slot != -1 && tid == 0) {
-                    flag(p.status, KDA_DEV_BAD_SLOT);
+            for (int i = 0; i < 64; ++i) S[i] = S0[(int64_t)(cbase + i) * kD + j];
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) S[i] = 0.f;
+        }
+        auto write_sa = [&]() {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const uint4 v = make_uint4(pack_bf16(S[8 * m], S[8 * m + 1]), pack_bf16(S[8 * m + 2], S[8 * m + 3]),
+                                           pack_bf16(S[8 * m + 4], S[8 * m + 5]), pack_bf16(S[8 * m + 6], S[8 * m + 7]));
+                sts16(s_base + kSa + kmajor_off(j, cbase + 8 * m, kD), v);
+            }
+            fence_async_smem();
+            mbar_arrive(&ms.bar_s);
+        };
+        write_sa();
+        bool ok = true;
+        for (int64_t lc = 0; lc < nc; ++lc) {
+            const uint32_t par = (uint32_t)(lc & 1);
+            const uint8_t* stage_p = sm + stage_of(lc);
+            if (!(ok = waitb(&ms.bar_load[lc & 1], (uint32_t)((lc >> 1) & 1)) && waitb(&ms.bar_ab, par))) break;
+            fence_after_sync();
+            // U^T = U~^T - D1 for this thread's 32 tokens
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t v[16];
+                tmem_ld16(tD1(lc) + lanebase + tq + 16 * hf, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e8 = 0; e8 < 2; ++e8) {
+                    const int cc = 4 * ch + 2 * hf + e8;
+                    const uint4 ut = *reinterpret_cast<const uint4*>(stage_p + kRecU + row64_chunk_off(j, cc));
+                    const uint32_t uw[4] = {ut.x, ut.y, ut.z, ut.w};
+                    uint32_t outw[4];
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+                        const float u0 = __uint_as_float(uw[e2] << 16) - __uint_as_float(v[8 * e8 + 2 * e2]);
+                        const float u1 = __uint_as_float(uw[e2] & 0xFFFF0000u) - __uint_as_float(v[8 * e8 + 2 * e2 + 1]);
+                        outw[e2] = pack_bf16(u0, u1);
+                    }
+                    st_shared_v4(s_base + kUa + row64_chunk_off(j, cc), outw[0], outw[1], outw[2], outw[3]);
                 }
+            }
+            fence_async_smem();
+            fence_before_sync();
+            mbar_arrive(&ms.bar_u);
+            if (!(ok = waitb(&ms.bar_d, par))) break;
+            fence_after_sync();
+            // S <- gamma * S + D3, then the bf16 copy for the next chunk
+            const float* gam = reinterpret_cast<const float*>(stage_p + kRecG) + cbase;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t v[16];
+                tmem_ld16(tD3 + lanebase + cbase + 16 * q4, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    S[16 * q4 + e] = fmaf(gam[16 * q4 + e], S[16 * q4 + e], __uint_as_float(v[e]));
+            }
+            fence_before_sync();
+            write_sa();
+            // snapshot after this chunk, straight from the fp32 registers
+            const int64_t t0 = tb + lc * kC;
+            const int n = (int)(te - t0 < kC ? te - t0 : kC);
+            const int64_t p_end = pos0 + lc * kC + n;
+            if (a.snap_table && p_end % a.snap_interval == 0) {
+                const int64_t ord = p_end / a.snap_interval - 1;
+                if (ord >= a.snap_table_stride) {
+                    if (tid == 0) flag(p.status, KDA_DEV_BAD_ORDINAL);
+                } else {
+                    const int32_t slot = a.snap_table[(int64_t)seq * a.snap_table_stride + ord];
+                    if (slot >= 0 && (int64_t)slot < a.n_slots) {
+                        float* dst = a.pool + (int64_t)slot * slot_stride + head_off;
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
+                    } else if (slot != -1 && tid == 0) {
+                        flag(p.status, KDA_DEV_BAD_SLOT);
+                    }
+                }
+            }
+        }
+        if (ok && a.final_state) {
+            float* dst = a.final_state + (int64_t)seq * slot_stride + head_off;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
+        }
+    } else {
+        // ------------------------------------------------------------------ output group
+        const int jq = warp & 3;
+        const int j = 32 * jq + lane;
+        const uint32_t lanebase = (uint32_t)(32 * jq) << 16;
+        __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
+        const int64_t ostride = (int64_t)H * kD;
+        for (int64_t lc = 0; lc < nc; ++lc) {
+            if (!waitb(&ms.bar_c, (uint32_t)(lc & 1))) break;
+            fence_after_sync();
+            uint32_t v[4][16];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tD2(lc) + lanebase + 16 * q4, v[q4]);
+            tmem_wait_ld();
+            fence_before_sync();
+            mbar_arrive(&ms.bar_o);
+            const int64_t t0 = tb + lc * kC;
+            const int n = (int)(te - t0 < kC ? te - t0 : kC);
+            __nv_bfloat16* orow = og + (t0 * H + h) * kD + j;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (16 * q4 + e < n)
+                        orow[(16 * q4 + e) * ostride] = __float2bfloat16_rn(a.scale * __uint_as_float(v[q4][e]));
             }
         }
     }
 
-    if (!ok) {
-        // let this CTA's own copies and MMAs in flight land (bounded) before
-        // the shared memory and tensor memory are released
-        if (tid == 0) {
-            flag(p.status, KDA_DEV_WAIT_TIMEOUT);
-            for (int st = 0; st < 2; ++st)
-                for (uint32_t l = ld_waited[st]; l < ld_issued[st]; ++l) mbar_wait(&ms.bar_load[st], l & 1);
-            for (uint32_t m = a_waited; m < a_issued; ++m) mbar_wait(&ms.bar_a, m & 1);
-            for (uint32_t m = cd_waited; m < cd_issued; ++m) mbar_wait(&ms.bar_cd, m & 1);
-        }
-    } else {
-        if (nc > 0) store_outputs(nc - 1);
-        if (a.final_state) {
-            float* dst = a.final_state + (int64_t)seq * slot_stride + head_off;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
-        }
-    }
+    if (ms.failed && tid == 0) flag(p.status, KDA_DEV_WAIT_TIMEOUT);
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
