@@ -17,7 +17,8 @@
 //   warp 12     one thread issues the record copies (two chunks in flight) and
 //               every MMA, in dependency order, through mbarriers.
 // [D1 | D2] is double-buffered in TMEM so the outputs of one chunk are read while
-// the next chunk's MMAs run.
+// the next chunk's MMAs run.  Every mbarrier wait is placed where the barrier can
+// be at most one phase ahead of it, as parity waits require.
 #include "chunk_common.cuh"
 
 namespace kda {
@@ -163,6 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
             for (int64_t lc = 0; lc < nc && ok; ++lc) {
                 const uint32_t par = (uint32_t)(lc & 1);
                 if (!(ok = waitb(&ms.bar_u, par))) break;          // U^T of lc written
+                // D2 of lc-1 read by the output group.  Waiting here, before (c) of
+                // lc is issued, keeps that barrier at most one phase ahead of this
+                // wait; the buffer is reused by (ab) of lc+1.
+                if (lc >= 1 && !(ok = waitb(&ms.bar_o, par ^ 1))) break;
                 fence_after_sync();
                 issue_dc(lc);
                 if (!(ok = waitb(&ms.bar_s, par ^ 1))) break;      // state after lc written
@@ -172,7 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
                 if (lc + 2 < nc) load(lc + 2);                      // record stage of lc is free
                 if (lc + 1 < nc) {
                     if (!(ok = wait_load(lc + 1))) break;
-                    if (lc >= 1 && !(ok = waitb(&ms.bar_o, (uint32_t)((lc - 1) & 1)))) break;   // D2 buffer free
                     issue_ab(lc + 1);
                 }
             }
