@@ -143,15 +143,24 @@ RECORDED_TRAFFIC = {}
 def barrier(dist_on):
     if dist_on:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(x, dist_on, dev):
+    """The largest of every rank's x (all ranks receive it)."""
     if not dist_on:
         return x
     t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(units_per_rank, local_ms, world, dist_on, dev):
+    """Whole-job throughput of `world` independent replicas: all ranks' units
+    over the slowest rank's time (units per second), and that time (ms)."""
+    slowest = max_over_ranks(local_ms, dist_on, dev)
+    return world * units_per_rank / (slowest / 1e3), slowest
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -249,9 +258,8 @@ def bench_ours(args, rank, world, dev, dist_on):
     barrier(dist_on)
     launches = kda.kda_launch_count() - launches0
     clk = clocks.stop()
-    total_ms = max_over_ranks(ev0.elapsed_time(ev1), dist_on, dev)
+    value, total_ms = replica_throughput(total * args.steps, ev0.elapsed_time(ev1), world, dist_on, dev)
     ms_per_step = total_ms / args.steps
-    value = world * total * args.steps / (total_ms / 1e3)
     assert kda.kda_check_status(stream) == 0
 
     stages = {}
