@@ -18,6 +18,10 @@ Contents
                    which absolute positions carry snapshots, and how much of a
                    shared prefix a snapshot grid lets a request reuse
                    ("Kimi K3 Tech Intro", sections 2.1-2.2).
+``PrefixCacheIndex`` / ``block_hashes``
+                   the prefix-cache policy: chained 256-token hashes, interval
+                   retention, second-hit admission, next-step reuse
+                   ("Kimi K3 Tech Intro", sections 2.2-2.4 and 3).
 ``window_bound``   a rigorous upper bound on how much a state that is forgotten
                    at the start of a window can change the states inside it,
                    used to check long sequences on sampled windows.
@@ -26,3 +30,4 @@ from .recurrent import run, threads, DT_BF16, DT_F32, DT_F64  # noqa: F401
 from .chunked import chunked  # noqa: F401
 from .positions import snapshot_positions, reusable_prefix  # noqa: F401
 from .bounds import window_bound, state_norm_bound  # noqa: F401
+from .prefix_cache import PrefixCacheIndex, block_hashes  # noqa: F401
