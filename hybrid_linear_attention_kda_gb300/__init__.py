@@ -17,7 +17,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "_lib", "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE_STATUS, \
-    KDA_ERR_TIMEOUT = range(6)
+    KDA_ERR_TIMEOUT, KDA_ERR_NO_MEMORY = range(7)
 KDA_BF16, KDA_FP32 = 0, 1
 KDA_DEV_BAD_SLOT, KDA_DEV_BAD_START, KDA_DEV_BAD_SEQLENS, KDA_DEV_BAD_ORDINAL = 0x1, 0x2, 0x4, 0x8
 
@@ -88,6 +88,8 @@ def load():
     lib.kda_snapshot_restore.argtypes = [vp, vp, i64, vp, i32, i32, i32, i32, vp]
     lib.kda_check_status.restype = ctypes.c_int
     lib.kda_check_status.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_uint32)]
+    from . import prefix_cache
+    prefix_cache.declare(lib)
     _lib = lib
     return lib
 

@@ -1,7 +1,8 @@
 """In-tree build of libkda.so (the C-ABI KDA library) for sm_103a.
 
-Each ``csrc/*.cu`` file compiles in its own nvcc process (in parallel), then one
-link step writes ``_lib/libkda.so``.  Nothing here runs a GPU: nvcc cross-compiles
+Each ``csrc/*.cu`` (device code) and ``csrc/*.cpp`` (host-only code) file
+compiles in its own nvcc process (in parallel), then one link step writes
+``_lib/libkda.so``.  Nothing here runs a GPU: nvcc cross-compiles
 on any host with the CUDA toolkit.
 """
 import concurrent.futures as cf
@@ -36,7 +37,7 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _headers():
@@ -67,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -165,6 +165,7 @@ const char* kda_status_string(kda_status_t s) {
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
         case KDA_ERR_DEVICE_STATUS: return "KDA_ERR_DEVICE_STATUS";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        case KDA_ERR_NO_MEMORY: return "KDA_ERR_NO_MEMORY";
     }
     return "KDA_ERR_UNKNOWN";
 }

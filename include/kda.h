@@ -72,7 +72,8 @@ typedef enum {
     KDA_ERR_UNSUPPORTED = 2,   /* shape or dtype outside the supported set */
     KDA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
     KDA_ERR_DEVICE_STATUS = 4, /* kda_check_status: a kernel flagged bad indices */
-    KDA_ERR_TIMEOUT = 5        /* kda_check_status: the stream did not drain in time */
+    KDA_ERR_TIMEOUT = 5,       /* kda_check_status: the stream did not drain in time */
+    KDA_ERR_NO_MEMORY = 6      /* host memory for a host-side structure could not be allocated */
 } kda_status_t;
 
 typedef enum {

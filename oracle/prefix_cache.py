@@ -181,10 +181,26 @@ class PrefixCacheIndex:
         if h is not None and h in self.entries:
             self.entries[h].pins -= 1
 
-    def lookup(self, hashes):
-        """Deepest published entry along a chain of hashes: (units, slot) or (0, -1)."""
-        for n in range(len(hashes), 0, -1):
-            e = self.entries.get(hashes[n - 1])
-            if e is not None and e.published:
-                return n, e.slot
-        return 0, -1
+    def lookup(self, h):
+        """Published entry with chained hash (logical id) h: (slot, position), or (-1, 0)."""
+        e = self.entries.get(h)
+        if e is not None and e.published:
+            return e.slot, e.pos
+        return -1, 0
+
+    def import_state(self, h, pos):
+        """Register a state that arrives from elsewhere under logical id h at
+        position pos.  Returns (slot, is_new): a new pending slot, or -1 when h is
+        already registered or no slot can be had."""
+        if pos < 1 or pos % self.unit != 0:
+            raise ValueError("bad position")
+        if h in self.entries:
+            return -1, False
+        self.clock += 1
+        slot = self._take_slot()
+        if slot is None:
+            self.dropped += 1
+            return -1, False
+        self.entries[h] = _Entry(slot, pos, self.clock)
+        self.pending.append(h)
+        return slot, True

@@ -38,7 +38,8 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ("kda_prefill_chunked", "kda_prefill_workspace_size", "kda_decode_step",
                      "kda_snapshot_gather", "kda_snapshot_restore", "kda_check_status",
-                     "kda_status_string"):
+                     "kda_status_string", "kda_pcache_create", "kda_pcache_plan_request",
+                     "kda_pcache_end_step", "kda_pcache_release"):
         assert required in names
 
 
@@ -56,6 +57,7 @@ def test_abi_version_and_status_strings(lib):
     assert kda.kda_abi_version() == 1
     assert kda.kda_status_string(kda.KDA_OK) == "KDA_OK"
     assert kda.kda_status_string(kda.KDA_ERR_TIMEOUT) == "KDA_ERR_TIMEOUT"
+    assert kda.kda_status_string(kda.KDA_ERR_NO_MEMORY) == "KDA_ERR_NO_MEMORY"
     assert kda.kda_status_string(99) == "KDA_ERR_UNKNOWN"
 
 
