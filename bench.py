@@ -433,11 +433,48 @@ def bench_ours(args, rank, world, dev, dist_on):
                           "ms_per_step": copy_ms, "states": 128},
         "kernel_fingerprint": fp,
     }
+    if rank == 0:
+        line["prefix_cache"] = bench_prefix_cache()
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         tps, cores, sample, _ = oracle_prefill_sample(host, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores,
                                 "kind": "oracle", "sample": sample}
     return line
+
+
+def bench_prefix_cache(n_req=2000, seed=20266):
+    """Host prefix-cache index on a synthetic serving stream: 16 system prompts of
+    2K-8K tokens, each request one of them plus a 100-2000-token question, one
+    step per 8 requests, second-hit admission, 32K-token interval retention."""
+    import numpy as np
+    from hybrid_linear_attention_kda_gb300.prefix_cache import PrefixCache
+    rng = np.random.default_rng(seed)
+    sys_prompts = [rng.integers(0, 163840, size=int(rng.integers(2048, 8192)), dtype=np.int32) for _ in range(16)]
+    reqs = [np.concatenate([sys_prompts[int(rng.integers(0, 16))],
+                            rng.integers(0, 163840, size=int(rng.integers(100, 2000)), dtype=np.int32)])
+            for _ in range(n_req)]
+    pc = PrefixCache(4096, retention_interval=32768, admit_on_second_hit=True)
+    row = np.full(64, -1, dtype=np.int32)
+    tokens = reused = 0
+    t0 = time.perf_counter()
+    ids = []
+    for i, r in enumerate(reqs):
+        p = pc.plan_request(r, snap_row=row)
+        ids.append(p["request_id"])
+        tokens += len(r)
+        reused += p["start_pos"]
+        if i % 8 == 7:
+            pc.end_step(True)
+            for rid in ids:
+                pc.release(rid)
+            ids = []
+    dt = time.perf_counter() - t0
+    st = pc.stats()
+    return {"workload": f"{n_req} requests over 16 shared system prompts (2K-8K tokens) + 100-2000-token "
+                        "questions, 8 per step, second-hit admission, 32K interval",
+            "value": n_req / dt, "unit": "plans/s", "us_per_plan": dt / n_req * 1e6,
+            "prompt_tokens_per_s": tokens / dt, "hit_rate": st["hits"] / max(1, st["requests"]),
+            "prompt_tokens_reused": reused / max(1, tokens), "host": "1 thread"}
 
 
 # ----------------------------------------------------------------------------- reference arm

@@ -130,6 +130,34 @@ WORKLOADS = {
 
 PREFIX_STREAM = 1_000_001
 LAYOUT_STREAM = 1_000_000
+TOKEN_TABLE_STREAM = 1_000_002
+
+
+def gen_token_table(vocab, H, d_k, d_v, seed, dtype=torch.bfloat16, decay="mild"):
+    """Layer inputs per token id, for serving-style runs driven by token ids.
+
+    Row t holds the q, k, v, alpha, beta that token id t feeds the layer (drawn
+    by the same recipe as above), a stand-in for the model's projections: equal
+    prompt prefixes then give equal layer inputs, which is what prefix reuse
+    relies on.  Returns dict of [vocab, H, .] tensors.
+    """
+    g = _stream(seed, TOKEN_TABLE_STREAM)
+    qb, kb, vb, ab, bb = gen_sequence_block(g, vocab, H, d_k, d_v, decay)
+    return {"q": qb.to(dtype), "k": kb.to(dtype), "v": vb.to(dtype),
+            "alpha": ab.to(torch.float32), "beta": bb.to(torch.float32)}
+
+
+def embed(table, token_lists):
+    """Packed inputs of several token-id lists: dict with q, k, v, alpha, beta
+    ([sum of lengths, H, .]) and cu_seqlens."""
+    lens = [len(t) for t in token_lists]
+    ids = torch.tensor([x for t in token_lists for x in t], dtype=torch.long)
+    out = {key: table[key].index_select(0, ids) for key in ("q", "k", "v", "alpha", "beta")}
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    if lens:
+        cu[1:] = torch.tensor(np.cumsum(lens), dtype=torch.int32)
+    out["cu_seqlens"] = cu
+    return out
 
 
 def torch_dtype(name):
