@@ -34,7 +34,7 @@ namespace kda {
 namespace {
 using namespace tc;
 
-constexpr int kThreads = 512;        // 16 warps; phase 1: one thread per (channel, 16-token quarter)
+constexpr int kThreads = 256;
 // shared memory (1024-aligned base)
 constexpr uint32_t kStageBytes = 81920;    // one input stage
 constexpr uint32_t kSq = 0, kSk = 16384, kSv = 32768, kSal = 49152;   // q, k, v bf16; alpha fp32 [64][128]
@@ -73,28 +73,6 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
 }
 __device__ __forceinline__ void sts16(uint32_t saddr, uint4 v) { st_shared_v4(saddr, v.x, v.y, v.z, v.w); }
 
-// Eight bf16 values gathered one at a time (index e = 0..7, any order) and
-// kept as packed pairs: a float waits only for its partner.
-struct Pack8 {
-    uint32_t w[4];
-    float pend;
-    __device__ __forceinline__ void put(int e, float x) {
-        if (e & 1) w[e >> 1] = pack_bf16(pend, x);
-        else pend = x;
-    }
-    __device__ __forceinline__ uint4 get() const { return make_uint4(w[0], w[1], w[2], w[3]); }
-};
-// The same for a walk in decreasing order (the odd element arrives first).
-struct Pack8Rev {
-    uint32_t w[4];
-    float pend;
-    __device__ __forceinline__ void put(int e, float x) {
-        if (e & 1) pend = x;
-        else w[e >> 1] = pack_bf16(x, pend);
-    }
-    __device__ __forceinline__ uint4 get() const { return make_uint4(w[0], w[1], w[2], w[3]); }
-};
-
 // byte offset of the 16-byte chunk (mn .. mn+7, k) of an MN-major tile
 __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
     return (k >> 3) * kSbo + (mn >> 6) * kLbo + (k & 7u) * 128u + ((((mn & 63u) >> 3) ^ (k & 7u)) << 4);
@@ -105,10 +83,9 @@ __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
 // 16 x 16 blocks below them inside each 32 x 32 diagonal block, then the lower
 // left 32 x 32 block, each off-diagonal block as
 //     T_ij = -T_ii (A_ij T_jj)       (for the block partition at that level).
-// All 512 threads take part; T (zeros above the diagonal inside the diagonal
+// All 256 threads take part; T (zeros above the diagonal inside the diagonal
 // blocks) goes to Tf, row-major.  scr holds 1024 floats.  Ends with a barrier.
 __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, float* scr, int tid) {
-    static_assert(kThreads == 512, "thread mapping");
     if (tid < kC) {
         const int o = 16 * (tid >> 4), jj = tid & 15;
         float t[16];
@@ -131,40 +108,45 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
         }
     }
     __syncthreads();
-    {   // blocks (1,0) and (3,2), one entry per thread: M = A_ij T_jj, then T_ij = -T_ii M
-        const int m = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
-        const int i = 1 + 2 * m, jb = i - 1;
-        const float* Ar = A + (16 * i + rr) * kC + 16 * jb;
-        float a0 = 0.f, a1 = 0.f;
+    {   // blocks (1,0) and (3,2): M = A_ij T_jj, then T_ij = -T_ii M
+        const int rr = tid >> 4, cc = tid & 15;
 #pragma unroll
-        for (int u = 0; u < 16; u += 2) {
-            a0 = fmaf(Ar[u], Tf[(16 * jb + u) * kC + 16 * jb + cc], a0);
-            a1 = fmaf(Ar[u + 1], Tf[(16 * jb + u + 1) * kC + 16 * jb + cc], a1);
+        for (int m = 0; m < 2; ++m) {
+            const int i = 1 + 2 * m, jb = i - 1;
+            const float* Ar = A + (16 * i + rr) * kC + 16 * jb;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; u += 2) {
+                a0 = fmaf(Ar[u], Tf[(16 * jb + u) * kC + 16 * jb + cc], a0);
+                a1 = fmaf(Ar[u + 1], Tf[(16 * jb + u + 1) * kC + 16 * jb + cc], a1);
+            }
+            scr[(m << 8) + tid] = a0 + a1;
         }
-        scr[tid] = a0 + a1;
         __syncthreads();
-        const float* Tr = Tf + (16 * i + rr) * kC + 16 * i;
-        a0 = 0.f;
-        a1 = 0.f;
 #pragma unroll
-        for (int u = 0; u < 16; u += 2) {
-            a0 = fmaf(Tr[u], scr[(m << 8) + (u << 4) + cc], a0);
-            a1 = fmaf(Tr[u + 1], scr[(m << 8) + ((u + 1) << 4) + cc], a1);
+        for (int m = 0; m < 2; ++m) {
+            const int i = 1 + 2 * m, jb = i - 1;
+            const float* Tr = Tf + (16 * i + rr) * kC + 16 * i;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; u += 2) {
+                a0 = fmaf(Tr[u], scr[(m << 8) + (u << 4) + cc], a0);
+                a1 = fmaf(Tr[u + 1], scr[(m << 8) + ((u + 1) << 4) + cc], a1);
+            }
+            Tf[(16 * i + rr) * kC + 16 * jb + cc] = -(a0 + a1);
         }
-        Tf[(16 * i + rr) * kC + 16 * jb + cc] = -(a0 + a1);
         __syncthreads();
     }
-    {   // lower-left 32 x 32 block, two entries per thread: M = A_LL T_00(32),
-        // then T_LL = -T_11(32) M
-        const int cc = tid & 31, r0 = tid >> 5;       // rows r0 and r0 + 16
-        float acc[2] = {0.f, 0.f};
+    {   // lower-left 32 x 32 block: M = A_LL T_00(32), then T_LL = -T_11(32) M
+        const int cc = tid & 31, r0 = tid >> 5;       // rows r0, r0 + 8, r0 + 16, r0 + 24
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int u = 0; u < 32; u += 4) {
             const float t0 = Tf[u * kC + cc], t1 = Tf[(u + 1) * kC + cc];
             const float t2 = Tf[(u + 2) * kC + cc], t3 = Tf[(u + 3) * kC + cc];
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const float4 a4 = *reinterpret_cast<const float4*>(A + (32 + r0 + 16 * m) * kC + u);
+            for (int m = 0; m < 4; ++m) {
+                const float4 a4 = *reinterpret_cast<const float4*>(A + (32 + r0 + 8 * m) * kC + u);
                 acc[m] = fmaf(a4.x, t0, acc[m]);
                 acc[m] = fmaf(a4.y, t1, acc[m]);
                 acc[m] = fmaf(a4.z, t2, acc[m]);
@@ -172,16 +154,17 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
             }
         }
 #pragma unroll
-        for (int m = 0; m < 2; ++m) scr[(r0 + 16 * m) * 32 + cc] = acc[m];
+        for (int m = 0; m < 4; ++m) scr[(r0 + 8 * m) * 32 + cc] = acc[m];
         __syncthreads();
-        acc[0] = acc[1] = 0.f;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) acc[m] = 0.f;
 #pragma unroll
         for (int u = 0; u < 32; u += 4) {
             const float s0 = scr[u * 32 + cc], s1 = scr[(u + 1) * 32 + cc];
             const float s2 = scr[(u + 2) * 32 + cc], s3 = scr[(u + 3) * 32 + cc];
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const float4 t4 = *reinterpret_cast<const float4*>(Tf + (32 + r0 + 16 * m) * kC + 32 + u);
+            for (int m = 0; m < 4; ++m) {
+                const float4 t4 = *reinterpret_cast<const float4*>(Tf + (32 + r0 + 8 * m) * kC + 32 + u);
                 acc[m] = fmaf(t4.x, s0, acc[m]);
                 acc[m] = fmaf(t4.y, s1, acc[m]);
                 acc[m] = fmaf(t4.z, s2, acc[m]);
@@ -189,7 +172,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
             }
         }
 #pragma unroll
-        for (int m = 0; m < 2; ++m) Tf[(32 + r0 + 16 * m) * kC + cc] = -acc[m];
+        for (int m = 0; m < 4; ++m) Tf[(32 + r0 + 8 * m) * kC + cc] = -acc[m];
         __syncthreads();
     }
 }
@@ -280,12 +263,8 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
     __syncthreads();
 
     const int c = tid & (kD - 1);
-    const int qq = tid >> 7;       // which 16-token quarter of the chunk this thread walks
-    const int hh = qq >> 1;        // its half
-    const int sub = qq & 1;        // 0: local tokens 0..15 of the half, 1: 16..31
-    const int lq = warp & 3;       // TMEM lane quarter of this warp
-    const int cg = warp >> 2;      // its 32-column group in the TMEM read-backs
-    const uint32_t lanebase = (uint32_t)(32 * lq) << 16;
+    const int hh = tid >> 7;       // which half of the chunk this thread walks
+    const uint32_t lanebase = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t apa = s_base + kAPa, apb = s_base + kAPb;
     bool ok = true;
     int k = 0;
@@ -311,116 +290,116 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         const uint16_t* sq = reinterpret_cast<const uint16_t*>(S + kSq);
         const uint16_t* sk = reinterpret_cast<const uint16_t*>(S + kSk);
         const uint16_t* sv = reinterpret_cast<const uint16_t*>(S + kSv);
-        const int r_base = 16 * qq;
-        float al[16];
-        uint32_t qp[8], kp[8], vq[8];
+        float al[32];
+        uint32_t qp[16], kp[16], vq[16];
+        float own = 1.f;
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-            const int r = r_base + i;
+        for (int i = 0; i < 32; i += 2) {
+            const int r = 32 * hh + i;
             const bool v0 = r < n, v1 = r + 1 < n;
             al[i] = v0 ? sal[r * kD + c] : 1.f;
             al[i + 1] = v1 ? sal[(r + 1) * kD + c] : 1.f;
             qp[i >> 1] = (v0 ? (uint32_t)sq[r * kD + c] : 0u) | ((v1 ? (uint32_t)sq[(r + 1) * kD + c] : 0u) << 16);
             kp[i >> 1] = (v0 ? (uint32_t)sk[r * kD + c] : 0u) | ((v1 ? (uint32_t)sk[(r + 1) * kD + c] : 0u) << 16);
             vq[i >> 1] = (v0 ? (uint32_t)sv[r * kD + c] : 0u) | ((v1 ? (uint32_t)sv[(r + 1) * kD + c] : 0u) << 16);
+            own *= al[i];
+            own *= al[i + 1];
         }
-        // the four quarter products of this channel (own one from registers)
-        float Qp[4];
+        // the other half's product; for half 0 also the product over tokens 32..47
+        float oth = 1.f, mid = 1.f;
 #pragma unroll
-        for (int qo = 0; qo < 4; ++qo) {
-            float prod = 1.f;
-            if (qo == qq) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) prod *= al[i];
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int r = 16 * qo + i;
-                    prod *= r < n ? sal[r * kD + c] : 1.f;
-                }
-            }
-            Qp[qo] = prod;
+        for (int i = 0; i < 32; ++i) {
+            const int r = 32 * (1 - hh) + i;
+            oth *= r < n ? sal[r * kD + c] : 1.f;
+            if (i == 15) mid = oth;
         }
-        float before = 1.f, after = 1.f;
-#pragma unroll
-        for (int qo = 0; qo < 4; ++qo) {
-            if (qo < qq) before *= Qp[qo];
-            if (qo > qq) after *= Qp[qo];
-        }
-        // xi_s = exp(g_47 - g_s) for s in half 0: own suffix x later quarters up to quarter 2
-        const float xi_rest = qq == 0 ? Qp[1] * Qp[2] : Qp[2];
-        if (qq == 0) reinterpret_cast<float*>(rec + kRecG)[c] = (Qp[0] * Qp[1]) * (Qp[2] * Qp[3]);
-        // the q, k, v and alpha tiles are consumed (q, v and alpha now hold X^T,
-        // Y^T and the staged Q~ / Kbar); the previous item's staged W / U~ must
-        // have left shared memory before the A/P operands overwrite it
+        const float H0 = hh ? oth : own, H1 = hh ? own : oth;
+        if (hh == 1) reinterpret_cast<float*>(rec + kRecG)[c] = H0 * H1;
+        // the q, v and alpha tiles are consumed (they now hold X^T, Y^T and the
+        // staged Q~ / Kbar); the previous item's staged W / U~ must have left
+        // shared memory before the A/P operands overwrite it
         if (tid == 0) bulk_wait_read();
         __syncthreads();
         const uint32_t qk_stage = Ss + kSal;      // Q~ tile, then Kbar tile
 
         bool guard_bad = false;
-        {   // forward: Gamma -> Q~ (record), X^T = beta Gamma k, Y^T = beta v; in the
-            // second quarter of a half also phi = E (inclusive prefix from local 16)
+        {   // forward: Gamma -> Q~ (record) and X^T = beta Gamma k (q tile); Y^T = beta v (v tile)
             float P = 1.f;
-            Pack8 gq, xk, yv, dq, dk, dd;
+            float gq[8], xk[8], yv[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 32; ++i) {
                 const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
                 const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
                 const float vf = (i & 1) ? bf_hi(vq[i >> 1]) : bf_lo(vq[i >> 1]);
-                const float b = bsm[r_base + i];
+                const float b = bsm[32 * hh + i];
                 P *= al[i];
-                const float G = before * P;
-                gq.put(i & 7, qf * G);
-                xk.put(i & 7, b * kf * G);
-                yv.put(i & 7, b * vf);
-                if (sub) {
-                    guard_bad |= !(P >= kGuardMin);
-                    const float inv = __fdividef(1.f, P);
-                    dq.put(i & 7, qf * P);
-                    dk.put(i & 7, kf * P);
-                    dd.put(i & 7, kf * inv);
-                }
+                const float G = hh ? H0 * P : P;
+                gq[i & 7] = qf * G;
+                xk[i & 7] = b * kf * G;
+                yv[i & 7] = b * vf;
                 if ((i & 7) == 7) {
-                    const uint32_t r0 = r_base + (i & ~7);
-                    sts16(qk_stage + row64_chunk_off(c, r0 >> 3), gq.get());
-                    sts16(Ss + kSq + row64_chunk_off(c, r0 >> 3), xk.get());
-                    sts16(Ss + kSv + row64_chunk_off(c, r0 >> 3), yv.get());
-                    if (sub) {
-                        sts16(apb + mn_chunk(r0, c), dq.get());
-                        sts16(apb + mn_chunk(64 + r0, c), dk.get());
-                        sts16(apa + mn_chunk(r0, c), dd.get());
-                    }
+                    const uint32_t cc = (32 * hh + (i & ~7)) >> 3;
+                    sts16(qk_stage + row64_chunk_off(c, cc), pack8(gq));
+                    sts16(Ss + kSq + row64_chunk_off(c, cc), pack8(xk));
+                    sts16(Ss + kSv + row64_chunk_off(c, cc), pack8(yv));
                 }
             }
         }
-        {   // backward: kappa -> Kbar (record); in the first quarter of a half also
-            // psi = D (exclusive suffix to local 15); in half 0 also xi
+        {   // forward from the half's reference token: phi = E, psi = 1/E (local tokens 16..31)
+            float E = 1.f;
+            float dq[8], dk[8], dd[8];
+#pragma unroll
+            for (int i = 16; i < 32; ++i) {
+                const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
+                const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+                E *= al[i];
+                guard_bad |= !(E >= kGuardMin);
+                const float inv = __fdividef(1.f, E);
+                dq[i & 7] = qf * E;
+                dk[i & 7] = kf * E;
+                dd[i & 7] = kf * inv;
+                if ((i & 7) == 7) {
+                    const uint32_t r0 = 32 * hh + (i & ~7);
+                    sts16(apb + mn_chunk(r0, c), pack8(dq));
+                    sts16(apb + mn_chunk(64 + r0, c), pack8(dk));
+                    sts16(apa + mn_chunk(r0, c), pack8(dd));
+                }
+            }
+        }
+        {   // backward: kappa (Kbar to the record); half 0 also xi = exp(g_47 - g_s)
             float Q = 1.f;
-            Pack8Rev kb, kx, dq, dk, dd;
+            float kb[8], kx[8];
+#pragma unroll
+            for (int i = 31; i >= 0; --i) {
+                const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+                kb[i & 7] = kf * (hh ? Q : Q * H1);
+                kx[i & 7] = kf * (Q * mid);
+                if ((i & 7) == 0) {
+                    sts16(qk_stage + 16384 + row64_chunk_off(c, (32 * hh + i) >> 3), pack8(kb));
+                    if (!hh) sts16(apa + mn_chunk(64 + i, c), pack8(kx));
+                }
+                Q *= al[i];
+            }
+        }
+        {   // backward to the half's reference token: phi = 1/D, psi = D (local tokens 0..15)
+            float Dd = 1.f;
+            float dq[8], dk[8], dd[8];
 #pragma unroll
             for (int i = 15; i >= 0; --i) {
                 const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
                 const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-                kb.put(i & 7, kf * (Q * after));
-                if (!hh) kx.put(i & 7, kf * (Q * xi_rest));
-                if (!sub) {
-                    guard_bad |= !(Q >= kGuardMin);
-                    const float inv = __fdividef(1.f, Q);
-                    dq.put(i & 7, qf * inv);
-                    dk.put(i & 7, kf * inv);
-                    dd.put(i & 7, kf * Q);
-                }
+                guard_bad |= !(Dd >= kGuardMin);
+                const float inv = __fdividef(1.f, Dd);
+                dq[i & 7] = qf * inv;
+                dk[i & 7] = kf * inv;
+                dd[i & 7] = kf * Dd;
                 if ((i & 7) == 0) {
-                    const uint32_t r0 = r_base + i;
-                    sts16(qk_stage + 16384 + row64_chunk_off(c, r0 >> 3), kb.get());
-                    if (!hh) sts16(apa + mn_chunk(64 + r0, c), kx.get());
-                    if (!sub) {
-                        sts16(apb + mn_chunk(r0, c), dq.get());
-                        sts16(apb + mn_chunk(64 + r0, c), dk.get());
-                        sts16(apa + mn_chunk(r0, c), dd.get());
-                    }
+                    const uint32_t r0 = 32 * hh + i;
+                    sts16(apb + mn_chunk(r0, c), pack8(dq));
+                    sts16(apb + mn_chunk(64 + r0, c), pack8(dk));
+                    sts16(apa + mn_chunk(r0, c), pack8(dd));
                 }
-                Q *= al[i];
+                Dd *= al[i];
             }
         }
         if (guard_bad) atomicOr(&ms.guard_fail, 1);
@@ -453,41 +432,45 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         fence_after_sync();
 
         // ------------------------------------------------------------ phase 2: P to the record, A to smem
-        // TMEM rows: 0..63 key token s (own-half reference), 64..95 key token s of
-        // half 0 (reference 47); columns 0..63 query token r, 64..127 key token r.
-        {
-            float* Am = reinterpret_cast<float*>(sm + kAmat);
-            // (lane quarter, column group) -> role
-            const bool p_load = (lq == 0 && cg == 0) || (lq == 1 && cg == 1) || (lq == 2 && cg == 1);
-            const bool a_load = (lq == 0 && cg == 2) || (lq == 1 && cg == 3) || (lq == 2 && cg == 3);
-            const int s = lq == 1 ? 32 + lane : lane;          // key token of this TMEM lane
-            if (p_load || a_load) {
-                const int col0 = 32 * cg;
-                uint32_t v[2][16];
-                tmem_ld16(tbase + lanebase + col0, v[0]);
-                tmem_ld16(tbase + lanebase + col0 + 16, v[1]);
+        if (warp < 3) {
+            const int s = warp == 2 ? lane : lane + 32 * warp;      // key token of this TMEM lane
+            const int col0 = warp == 0 ? 0 : 32;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t v[16];
+                tmem_ld16(tbase + lanebase + col0 + 16 * hf, v);
                 tmem_wait_ld();
-                if (p_load) {
 #pragma unroll
-                    for (int e8 = 0; e8 < 4; ++e8) {
-                        const int r0 = col0 + 8 * e8;               // query tokens r0 .. r0+7
-                        float x[8];
+                for (int e8 = 0; e8 < 2; ++e8) {
+                    const int r0 = col0 + 16 * hf + 8 * e8;
+                    float x[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            x[e] = (lq == 2 || r0 + e >= s) ? __uint_as_float(v[e8 >> 1][8 * (e8 & 1) + e]) : 0.f;
-                        sts16(s_base + kPst + row64_chunk_off(s, r0 >> 3), pack8(x));
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int r = col0 - 64 + e;                // key token r
-                        Am[r * kC + s] = (lq == 2 || r > s) ? bsm[r] * __uint_as_float(v[e >> 4][e & 15]) : 0.f;
-                    }
+                    for (int e = 0; e < 8; ++e)
+                        x[e] = (warp == 2 || r0 + e >= s) ? __uint_as_float(v[8 * e8 + e]) : 0.f;
+                    sts16(s_base + kPst + row64_chunk_off(s, r0 >> 3), pack8(x));
                 }
-            } else if (lq == 1 && cg == 0) {
+            }
+            if (warp == 1) {
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) sts16(s_base + kPst + row64_chunk_off(s, cc), make_uint4(0u, 0u, 0u, 0u));
-            } else if (lq == 1 && cg == 2) {
+            }
+        } else if (warp >= 4 && warp < 7) {
+            const int wq = warp - 4;
+            const int s = wq == 2 ? lane : lane + 32 * wq;
+            const int col0 = wq == 0 ? 64 : 96;                     // columns 64 + r
+            float* Am = reinterpret_cast<float*>(sm + kAmat);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t v[16];
+                tmem_ld16(tbase + lanebase + col0 + 16 * hf, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int r = col0 - 64 + 16 * hf + e;
+                    Am[r * kC + s] = (wq == 2 || r > s) ? bsm[r] * __uint_as_float(v[e]) : 0.f;
+                }
+            }
+            if (wq == 1) {
                 for (int r = 0; r < 32; ++r) Am[r * kC + s] = 0.f;
             }
         }
@@ -505,14 +488,18 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
                           reinterpret_cast<float*>(sm + kTscr), tid);
         {   // T^T row s (= column s of T, zero above the diagonal) as the MN-major [s][r] operand
             const float* Tf = reinterpret_cast<const float*>(sm + kTf);
-            const int srow = tid >> 3, cc = tid & 7;
-            float x[8];
+            const int srow = tid >> 2;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int r = 8 * cc + e;
-                x[e] = r >= srow ? Tf[r * kC + srow] : 0.f;
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int cc = 2 * (tid & 3) + q2;
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int r = 8 * cc + e;
+                    x[e] = r >= srow ? Tf[r * kC + srow] : 0.f;
+                }
+                sts16(s_base + kTm + row64_chunk_off(srow, cc), pack8(x));
             }
-            sts16(s_base + kTm + row64_chunk_off(srow, cc), pack8(x));
         }
         fence_async_smem();
         fence_before_sync();
@@ -547,19 +534,21 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
 
         // ------------------------------------------------------------ phase 4: W and U~ to the record
         {
-            const int row = 32 * lq + lane;
-            const uint32_t col0 = 32 * cg;                         // W: 0..63, U~: 64..127
-            const uint32_t dst = s_base + kWst + (cg < 2 ? 0u : 16384u);
-            uint32_t v[2][16];
-            tmem_ld16(tbase + lanebase + col0, v[0]);
-            tmem_ld16(tbase + lanebase + col0 + 16, v[1]);
-            tmem_wait_ld();
+            const int row = 32 * (warp & 3) + lane;
+            const uint32_t col0 = warp < 4 ? 0u : 64u;
+            const uint32_t dst = s_base + kWst + (warp < 4 ? 0u : 16384u);
 #pragma unroll
-            for (int e8 = 0; e8 < 4; ++e8) {
-                float x[8];
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t v[16];
+                tmem_ld16(tbase + lanebase + col0 + 16 * q4, v);
+                tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[e8 >> 1][8 * (e8 & 1) + e]);
-                sts16(dst + row64_chunk_off(row, 4 * (cg & 1) + e8), pack8(x));
+                for (int e8 = 0; e8 < 2; ++e8) {
+                    float x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * e8 + e]);
+                    sts16(dst + row64_chunk_off(row, 2 * q4 + e8), pack8(x));
+                }
             }
         }
         // beta of the next item into its buffer; start loading the one after

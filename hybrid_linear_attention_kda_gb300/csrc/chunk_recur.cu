@@ -212,9 +212,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
                 sts16(s_base + kSa + kmajor_off(j, cbase + 8 * m, kD), v);
             }
             fence_async_smem();
-            // a snapshot staged in a record stage must have been read out before
-            // this phase lets the issuer refill that stage
-            if (tid == 0) bulk_wait_read();
             mbar_arrive(&ms.bar_s);
         };
         write_sa();
@@ -251,53 +248,34 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
             if (!(ok = waitb(&ms.bar_d, par))) break;
             fence_after_sync();
             // S <- gamma * S + D3, then the bf16 copy for the next chunk
-            const float4* gam4 = reinterpret_cast<const float4*>(stage_p + kRecG) + cbase / 4;
+            const float* gam = reinterpret_cast<const float*>(stage_p + kRecG) + cbase;
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 uint32_t v[16];
                 tmem_ld16(tD3 + lanebase + cbase + 16 * q4, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e4 = 0; e4 < 4; ++e4) {
-                    const float4 g = gam4[4 * q4 + e4];
-                    float* Sx = S + 16 * q4 + 4 * e4;
-                    Sx[0] = fmaf(g.x, Sx[0], __uint_as_float(v[4 * e4 + 0]));
-                    Sx[1] = fmaf(g.y, Sx[1], __uint_as_float(v[4 * e4 + 1]));
-                    Sx[2] = fmaf(g.z, Sx[2], __uint_as_float(v[4 * e4 + 2]));
-                    Sx[3] = fmaf(g.w, Sx[3], __uint_as_float(v[4 * e4 + 3]));
-                }
+                for (int e = 0; e < 16; ++e)
+                    S[16 * q4 + e] = fmaf(gam[16 * q4 + e], S[16 * q4 + e], __uint_as_float(v[e]));
             }
             fence_before_sync();
             write_sa();
-            // snapshot after this chunk: the fp32 state is staged in the record
-            // stage's first 64 KiB (W, Q~, Kbar and U~ are consumed once (d) is
-            // done; P, still read by (c), lies beyond) in the pool's [c][j]
-            // layout and leaves by one bulk copy
+            // snapshot after this chunk, straight from the fp32 registers
             const int64_t t0 = tb + lc * kC;
             const int n = (int)(te - t0 < kC ? te - t0 : kC);
             const int64_t p_end = pos0 + lc * kC + n;
             if (a.snap_table && p_end % a.snap_interval == 0) {
                 const int64_t ord = p_end / a.snap_interval - 1;
-                int32_t slot = -1;
                 if (ord >= a.snap_table_stride) {
                     if (tid == 0) flag(p.status, KDA_DEV_BAD_ORDINAL);
                 } else {
-                    slot = a.snap_table[(int64_t)seq * a.snap_table_stride + ord];
-                    if (slot != -1 && (slot < 0 || (int64_t)slot >= a.n_slots)) {
-                        if (tid == 0) flag(p.status, KDA_DEV_BAD_SLOT);
-                        slot = -1;
-                    }
-                }
-                if (slot >= 0) {
-                    static_assert(kRecP >= (uint32_t)kD * kD * 4, "snapshot staging overlaps P");
-                    float* stg = reinterpret_cast<float*>(sm + stage_of(lc));
+                    const int32_t slot = a.snap_table[(int64_t)seq * a.snap_table_stride + ord];
+                    if (slot >= 0 && (int64_t)slot < a.n_slots) {
+                        float* dst = a.pool + (int64_t)slot * slot_stride + head_off;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) stg[(cbase + i) * kD + j] = S[i];
-                    fence_async_smem();
-                    asm volatile("bar.sync 1, %0;" ::"r"(32 * kStateWarps) : "memory");   // state group only
-                    if (tid == 0) {
-                        bulk_s2g(a.pool + (int64_t)slot * slot_stride + head_off, stg, kD * kD * 4);
-                        bulk_commit();
+                        for (int i = 0; i < 64; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
+                    } else if (slot != -1 && tid == 0) {
+                        flag(p.status, KDA_DEV_BAD_SLOT);
                     }
                 }
             }
@@ -307,7 +285,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
 #pragma unroll
             for (int i = 0; i < 64; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
         }
-        if (tid == 0) bulk_wait_all();      // staged snapshots written out
     } else {
         // ------------------------------------------------------------------ output group
         const int jq = warp & 3;
