@@ -1,12 +1,16 @@
 // Stage one of the chunked prefill: everything of a 64-token chunk that does not
 // depend on the carried state, for all (chunk, head) pairs.
 //
-// A persistent kernel: one CTA per SM walks its share of the (chunk, head) items.
-// The items' q, k, v and alpha tiles ([64 tokens x 128 channels], token rows
-// H*128 elements apart in the packed tensors) arrive by TMA tensor copies into
-// two input stages, so the next item's 80 KiB are in flight while the current
-// item is computed.  Record tiles are staged in shared memory and leave by bulk
-// copies; X^T and Y^T are built in place of the q and v tiles once those are read.
+// A persistent kernel with two co-resident CTAs per SM, each walking its share of
+// the (chunk, head) items one at a time: the phases of one CTA (gate products,
+// MMA waits, the fp32 inversion, the load of its next item) run beside those of
+// the other.  An item's q, k and alpha tiles ([64 tokens x 128 channels], token
+// rows H*128 elements apart in the packed tensors) arrive by TMA tensor copies;
+// v arrives in the 128-byte-swizzled layout the tensor cores read, as two
+// [64 tokens x 64 channels] boxes, and is the A operand of the U~ product as it
+// lies.  Once q, k and alpha sit in registers their 64 KiB hold the A/P
+// operands, then A and T.  Q~ and Kbar go from registers to the record; P, W and
+// U~ are staged in shared memory and leave by bulk copies.
 //
 // Decay factors are products of alphas over token ranges (no exp / log): with
 // the chunk split into halves of 32 tokens and m the 16th token of a half,
@@ -25,7 +29,7 @@
 // psi span at most 16 tokens; a chunk whose factors leave [2^-100, 2^100] flags
 // its (sequence, head) for the token-serial kernel.  T = (I + A)^-1 is inverted
 // by 16 x 16 blocks in fp32, then W and U~ come from a second MMA
-// (X^T T^T and Y^T T^T with X = diag(beta) Gamma K, Y = diag(beta) V).
+// (X^T T'^T and V^T T'^T with X = Gamma K and T' = T diag(beta)).
 #include <cuda.h>
 
 #include "chunk_common.cuh"
@@ -35,31 +39,41 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 256;
-// shared memory (1024-aligned base)
-constexpr uint32_t kStageBytes = 81920;    // one input stage
-constexpr uint32_t kSq = 0, kSk = 16384, kSv = 32768, kSal = 49152;   // q, k, v bf16; alpha fp32 [64][128]
-constexpr uint32_t kR = 2 * kStageBytes;   // A/P operands, then A / T scratch
-constexpr uint32_t kAPa = kR;              // MN-major [c][128 rows s]
-constexpr uint32_t kAPb = kR + 32768;      // MN-major [c][128 cols r]
+constexpr int kCtasPerSm = 2;              // two co-resident CTAs overlap each other's phases
+// Shared memory of one CTA (1024-aligned base), one item at a time.  Channels are
+// taken in two rounds of 64; round g's q, k and alpha boxes ([64 tokens][64
+// channels], no swizzle) fill region g, which then takes the round's K-slices
+// of the A/P operands (channels 64g .. 64g+63).
+constexpr uint32_t kRound = 32768;         // region g at g * kRound
+constexpr uint32_t kRq = 0, kRk = 8192, kRal = 16384;      // q, k bf16 [64][64]; alpha fp32 [64][64]
+constexpr uint32_t kRa = 0, kRb = 16384;   // APa / APb K-slices: MN-major [8-channel group][128 rows]
+constexpr uint32_t kSv = 65536;            // v: two 128-byte-swizzled [64 t][64 c] boxes, 8 KiB apart
+constexpr uint32_t kVbox = 8192;
+constexpr uint32_t kX = 81920;             // X^T = (Gamma k)^T, K-major [c][t]
+constexpr uint32_t kLoadBytes = 81920;     // q, k, v and alpha of one item
 constexpr uint32_t kLbo = 1024, kSbo = 2048;
-constexpr uint32_t kAmat = kR;             // after the A/P MMA: A fp32 [64][64]
-constexpr uint32_t kTf = kR + 16384;       //   T fp32 [64][64]
-constexpr uint32_t kTscr = kR + 32768;     //   block-product scratch, 1024 fp32
-constexpr uint32_t kTm = kR + 36864;       //   T^T bf16, MN-major [s][r]
-constexpr uint32_t kPst = kR + 45056;      //   P record tile, staged for its bulk store
-constexpr uint32_t kWst = kR;              // after the W/U~ MMA: W and U~ record tiles, staged
-constexpr uint32_t kMisc = kR + 65536;
+// [0, 64 KiB) once the A/P MMA has read its operands:
+constexpr uint32_t kAmat = 0;              // A fp32 [64][64]
+constexpr uint32_t kTf = 16384;            // T fp32 [64][64]
+constexpr uint32_t kTscr = 32768;          // block-product scratch, 1024 fp32
+constexpr uint32_t kTm = 36864;            // (T diag(beta))^T bf16, MN-major [s][r]
+constexpr uint32_t kPst = 45056;           // P record tile, staged for its bulk store
+constexpr uint32_t kWst = 0;               // after the W/U~ MMA: W and U~ record tiles, staged
+constexpr uint32_t kMisc = 98304;
 constexpr uint32_t kTmemCols = 128;
 
 struct Misc {
-    float beta[2][kC];
-    uint64_t bar_load[2];
+    float beta[kC];
+    float qprod[2][4][64];     // per round: product of alpha over each 16-token quarter, per channel
+    uint64_t bar_load;
     uint64_t bar_mma;
     uint32_t tslot;
     int32_t guard_fail;
+    // copies and MMAs thread 0 issued and waited for, to drain on a timeout
+    uint32_t ld_issued, ld_waited, mma_issued, mma_waited;
 };
 constexpr size_t kSmemBytes = kMisc + sizeof(Misc) + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
 
 struct LocalMaps {
     CUtensorMap q, k, v, alpha;   // 2-D views [T_tot rows x H*128 elements]
@@ -72,6 +86,29 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
                       pack_bf16(v[6], v[7]));
 }
 __device__ __forceinline__ void sts16(uint32_t saddr, uint4 v) { st_shared_v4(saddr, v.x, v.y, v.z, v.w); }
+__device__ __forceinline__ void stg16(uint8_t* gaddr, uint4 v) { *reinterpret_cast<uint4*>(gaddr) = v; }
+
+// Eight bf16 values gathered one at a time (index e = 0..7, ascending) and kept
+// as packed pairs: a float waits only for its partner.
+struct Pack8 {
+    uint32_t w[4];
+    float pend;
+    __device__ __forceinline__ void put(int e, float x) {
+        if (e & 1) w[e >> 1] = pack_bf16(pend, x);
+        else pend = x;
+    }
+    __device__ __forceinline__ uint4 get() const { return make_uint4(w[0], w[1], w[2], w[3]); }
+};
+// The same for a walk in decreasing order (the odd element arrives first).
+struct Pack8Rev {
+    uint32_t w[4];
+    float pend;
+    __device__ __forceinline__ void put(int e, float x) {
+        if (e & 1) pend = x;
+        else w[e >> 1] = pack_bf16(x, pend);
+    }
+    __device__ __forceinline__ uint4 get() const { return make_uint4(w[0], w[1], w[2], w[3]); }
+};
 
 // byte offset of the 16-byte chunk (mn .. mn+7, k) of an MN-major tile
 __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
@@ -201,7 +238,7 @@ __device__ __forceinline__ Item decode_item(const ChunkLaunch& p, int64_t item, 
     return it;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant__ LocalMaps tm) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -218,30 +255,26 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
 
     if (warp == 0) tmem_alloc(&ms.tslot, kTmemCols);
     if (tid == 0) {
-        mbar_init(&ms.bar_load[0], 1);
-        mbar_init(&ms.bar_load[1], 1);
+        mbar_init(&ms.bar_load, 1);
         mbar_init(&ms.bar_mma, 1);
         ms.guard_fail = 0;
+        ms.ld_issued = ms.ld_waited = ms.mma_issued = ms.mma_waited = 0;
         fence_mbar_init();
     }
     // thread 0 issues every copy and MMA and counts them, to drain on a timeout
-    uint32_t ld_issued[2] = {0, 0}, ld_waited[2] = {0, 0}, mma_issued = 0, mma_waited = 0;
-    auto issue_load = [&](int64_t item, int4 info, int st) {
+    auto issue_load = [&](int64_t item, int4 info) {
         const Item it = decode_item(p, item, info);
-        uint8_t* S = sm + st * kStageBytes;
-        mbar_expect_tx(&ms.bar_load[st], kStageBytes);
+        mbar_expect_tx(&ms.bar_load, kLoadBytes);
         const int32_t x = it.h * kD, y = (int32_t)it.t0;
-        tma_load_2d(S + kSq, &tm.q, x, y, &ms.bar_load[st]);
-        tma_load_2d(S + kSk, &tm.k, x, y, &ms.bar_load[st]);
-        tma_load_2d(S + kSv, &tm.v, x, y, &ms.bar_load[st]);
-        tma_load_2d(S + kSal, &tm.alpha, x, y, &ms.bar_load[st]);
-        ld_issued[st] += 1;
-    };
-    // beta of an item, one token per thread tid < 64
-    auto load_beta = [&](int64_t item, int4 info) -> float {
-        if (tid >= kC || item >= n_items) return 0.f;
-        const Item it = decode_item(p, item, info);
-        return tid < it.n ? a.beta[(it.t0 + tid) * H + it.h] : 0.f;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            uint8_t* R = sm + g * kRound;
+            tma_load_2d(R + kRq, &tm.q, x + 64 * g, y, &ms.bar_load);
+            tma_load_2d(R + kRk, &tm.k, x + 64 * g, y, &ms.bar_load);
+            tma_load_2d(R + kRal, &tm.alpha, x + 64 * g, y, &ms.bar_load);
+            tma_load_2d(sm + kSv + g * kVbox, &tm.v, x + 64 * g, y, &ms.bar_load);
+        }
+        ms.ld_issued += 1;
     };
     fence_before_sync();
     __syncthreads();
@@ -253,153 +286,128 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm.v)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm.alpha)) : "memory");
     }
-    int4 info_cur = item_info(p, first, n_items), info_nxt = item_info(p, first + step, n_items);
-    if (tid == 0) {
-        issue_load(first, info_cur, 0);
-        if (first + step < n_items) issue_load(first + step, info_nxt, 1);
-    }
-    if (tid < kC) ms.beta[0][tid] = load_beta(first, info_cur);
-    float beta_next = load_beta(first + step, info_nxt);
+    if (tid == 0) issue_load(first, item_info(p, first, n_items));
     __syncthreads();
 
-    const int c = tid & (kD - 1);
-    const int hh = tid >> 7;       // which half of the chunk this thread walks
+    const int cl = tid & 63;       // channel within a round
+    const int qq = tid >> 6;       // which 16-token quarter of the chunk this thread walks
+    const int hh = qq >> 1;        // its half
+    const int sub = qq & 1;        // 0: local tokens 0..15 of the half, 1: 16..31
     const uint32_t lanebase = (uint32_t)(32 * (warp & 3)) << 16;
-    const uint32_t apa = s_base + kAPa, apb = s_base + kAPb;
     bool ok = true;
     int k = 0;
     for (int64_t item = first; item < n_items; item += step, ++k) {
-        const int st = k & 1;
-        const int4 info_nxt2 = item_info(p, item + 2 * step, n_items);   // used at the end of this item
-        const Item it = decode_item(p, item, info_cur);
+        const Item it = decode_item(p, item, item_info(p, item, n_items));
         const int n = it.n;
         uint8_t* rec = p.records + ((size_t)it.g * H + it.h) * kRecBytes;
-        const uint8_t* S = sm + st * kStageBytes;
-        const uint32_t Ss = s_base + st * kStageBytes;
-        const float* bsm = ms.beta[st];
+        const float* bsm = ms.beta;
+        // beta of this item (first read after the A/P MMA, several barriers on)
+        if (tid < kC) ms.beta[tid] = tid < n ? a.beta[(it.t0 + tid) * H + it.h] : 0.f;
 
-        ok = mbar_wait(&ms.bar_load[st], (uint32_t)((k >> 1) & 1));
-        if (tid == 0 && ok) ld_waited[st] += 1;
+        ok = mbar_wait(&ms.bar_load, (uint32_t)(k & 1));
+        if (tid == 0 && ok) ms.ld_waited += 1;
         if (__syncthreads_or(!ok)) {
             ok = false;
             break;
         }
 
         // ------------------------------------------------------------ phase 1: gates, operands
-        const float* sal = reinterpret_cast<const float*>(S + kSal);
-        const uint16_t* sq = reinterpret_cast<const uint16_t*>(S + kSq);
-        const uint16_t* sk = reinterpret_cast<const uint16_t*>(S + kSk);
-        const uint16_t* sv = reinterpret_cast<const uint16_t*>(S + kSv);
-        float al[32];
-        uint32_t qp[16], kp[16], vq[16];
-        float own = 1.f;
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            const int r = 32 * hh + i;
-            const bool v0 = r < n, v1 = r + 1 < n;
-            al[i] = v0 ? sal[r * kD + c] : 1.f;
-            al[i + 1] = v1 ? sal[(r + 1) * kD + c] : 1.f;
-            qp[i >> 1] = (v0 ? (uint32_t)sq[r * kD + c] : 0u) | ((v1 ? (uint32_t)sq[(r + 1) * kD + c] : 0u) << 16);
-            kp[i >> 1] = (v0 ? (uint32_t)sk[r * kD + c] : 0u) | ((v1 ? (uint32_t)sk[(r + 1) * kD + c] : 0u) << 16);
-            vq[i >> 1] = (v0 ? (uint32_t)sv[r * kD + c] : 0u) | ((v1 ? (uint32_t)sv[(r + 1) * kD + c] : 0u) << 16);
-            own *= al[i];
-            own *= al[i + 1];
-        }
-        // the other half's product; for half 0 also the product over tokens 32..47
-        float oth = 1.f, mid = 1.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int r = 32 * (1 - hh) + i;
-            oth *= r < n ? sal[r * kD + c] : 1.f;
-            if (i == 15) mid = oth;
-        }
-        const float H0 = hh ? oth : own, H1 = hh ? own : oth;
-        if (hh == 1) reinterpret_cast<float*>(rec + kRecG)[c] = H0 * H1;
-        // the q, v and alpha tiles are consumed (they now hold X^T, Y^T and the
-        // staged Q~ / Kbar); the previous item's staged W / U~ must have left
-        // shared memory before the A/P operands overwrite it
-        if (tid == 0) bulk_wait_read();
-        __syncthreads();
-        const uint32_t qk_stage = Ss + kSal;      // Q~ tile, then Kbar tile
-
+        // Decay factors of channel c for the quarter's tokens, with m the 16th
+        // token of the half: Gamma (chunk prefix), kappa (chunk suffix),
+        // phi = exp(g_r - g_m) and psi = 1/phi (sub 1 walks up from m, sub 0
+        // down to it), xi = exp(g_47 - g_s) for half 0.
         bool guard_bad = false;
-        {   // forward: Gamma -> Q~ (record) and X^T = beta Gamma k (q tile); Y^T = beta v (v tile)
-            float P = 1.f;
-            float gq[8], xk[8], yv[8];
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+            const int c = 64 * g + cl;
+            const uint8_t* R = sm + g * kRound;
+            const uint32_t Rs = s_base + g * kRound;
+            const float* sal = reinterpret_cast<const float*>(R + kRal);
+            const uint16_t* sq = reinterpret_cast<const uint16_t*>(R + kRq);
+            const uint16_t* sk = reinterpret_cast<const uint16_t*>(R + kRk);
+            const int r_base = 16 * qq;
+            float al[16];
+            uint32_t qp[8], kp[8];
+            float own = 1.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
-                const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-                const float vf = (i & 1) ? bf_hi(vq[i >> 1]) : bf_lo(vq[i >> 1]);
-                const float b = bsm[32 * hh + i];
-                P *= al[i];
-                const float G = hh ? H0 * P : P;
-                gq[i & 7] = qf * G;
-                xk[i & 7] = b * kf * G;
-                yv[i & 7] = b * vf;
-                if ((i & 7) == 7) {
-                    const uint32_t cc = (32 * hh + (i & ~7)) >> 3;
-                    sts16(qk_stage + row64_chunk_off(c, cc), pack8(gq));
-                    sts16(Ss + kSq + row64_chunk_off(c, cc), pack8(xk));
-                    sts16(Ss + kSv + row64_chunk_off(c, cc), pack8(yv));
+            for (int i = 0; i < 16; i += 2) {
+                const int r = r_base + i;
+                const bool v0 = r < n, v1 = r + 1 < n;
+                al[i] = v0 ? sal[r * 64 + cl] : 1.f;
+                al[i + 1] = v1 ? sal[(r + 1) * 64 + cl] : 1.f;
+                qp[i >> 1] = (v0 ? (uint32_t)sq[r * 64 + cl] : 0u) | ((v1 ? (uint32_t)sq[(r + 1) * 64 + cl] : 0u) << 16);
+                kp[i >> 1] = (v0 ? (uint32_t)sk[r * 64 + cl] : 0u) | ((v1 ? (uint32_t)sk[(r + 1) * 64 + cl] : 0u) << 16);
+                own *= al[i];
+                own *= al[i + 1];
+            }
+            ms.qprod[g][qq][cl] = own;
+            // every thread holds its inputs: region g now takes the operand slices
+            __syncthreads();
+            const float Q0 = ms.qprod[g][0][cl], Q1 = ms.qprod[g][1][cl];
+            const float Q2 = ms.qprod[g][2][cl], Q3 = ms.qprod[g][3][cl];
+            const float before = qq == 0 ? 1.f : qq == 1 ? Q0 : qq == 2 ? Q0 * Q1 : (Q0 * Q1) * Q2;
+            const float after = qq == 3 ? 1.f : qq == 2 ? Q3 : qq == 1 ? Q2 * Q3 : Q1 * (Q2 * Q3);
+            const float xi_rest = qq == 0 ? Q1 * Q2 : Q2;      // tokens after the quarter, up to 47
+            if (qq == 0) reinterpret_cast<float*>(rec + kRecG)[c] = (Q0 * Q1) * (Q2 * Q3);
+            const uint32_t apa = Rs + kRa, apb = Rs + kRb;
+            {   // forward: Gamma -> Q~ (record), X^T = Gamma k; in sub 1 also phi, psi
+                float P = 1.f;
+                Pack8 gq, xk, dq, dk, dd;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
+                    const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+                    P *= al[i];
+                    const float G = before * P;
+                    gq.put(i & 7, qf * G);
+                    xk.put(i & 7, kf * G);
+                    if (sub) {
+                        guard_bad |= !(P >= kGuardMin);
+                        const float inv = __fdividef(1.f, P);
+                        dq.put(i & 7, qf * P);
+                        dk.put(i & 7, kf * P);
+                        dd.put(i & 7, kf * inv);
+                    }
+                    if ((i & 7) == 7) {
+                        const uint32_t r0 = r_base + (i & ~7);
+                        stg16(rec + kRecQ + row64_chunk_off(c, r0 >> 3), gq.get());
+                        sts16(s_base + kX + row64_chunk_off(c, r0 >> 3), xk.get());
+                        if (sub) {
+                            sts16(apb + mn_chunk(r0, cl), dq.get());
+                            sts16(apb + mn_chunk(64 + r0, cl), dk.get());
+                            sts16(apa + mn_chunk(r0, cl), dd.get());
+                        }
+                    }
                 }
             }
-        }
-        {   // forward from the half's reference token: phi = E, psi = 1/E (local tokens 16..31)
-            float E = 1.f;
-            float dq[8], dk[8], dd[8];
+            {   // backward: kappa -> Kbar (record); half 0 also xi; in sub 0 also phi, psi
+                float Q = 1.f;
+                Pack8Rev kb, kx, dq, dk, dd;
 #pragma unroll
-            for (int i = 16; i < 32; ++i) {
-                const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
-                const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-                E *= al[i];
-                guard_bad |= !(E >= kGuardMin);
-                const float inv = __fdividef(1.f, E);
-                dq[i & 7] = qf * E;
-                dk[i & 7] = kf * E;
-                dd[i & 7] = kf * inv;
-                if ((i & 7) == 7) {
-                    const uint32_t r0 = 32 * hh + (i & ~7);
-                    sts16(apb + mn_chunk(r0, c), pack8(dq));
-                    sts16(apb + mn_chunk(64 + r0, c), pack8(dk));
-                    sts16(apa + mn_chunk(r0, c), pack8(dd));
+                for (int i = 15; i >= 0; --i) {
+                    const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
+                    const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+                    kb.put(i & 7, kf * (Q * after));
+                    if (!hh) kx.put(i & 7, kf * (Q * xi_rest));
+                    if (!sub) {
+                        guard_bad |= !(Q >= kGuardMin);
+                        const float inv = __fdividef(1.f, Q);
+                        dq.put(i & 7, qf * inv);
+                        dk.put(i & 7, kf * inv);
+                        dd.put(i & 7, kf * Q);
+                    }
+                    if ((i & 7) == 0) {
+                        const uint32_t r0 = r_base + i;
+                        stg16(rec + kRecK + row64_chunk_off(c, r0 >> 3), kb.get());
+                        if (!hh) sts16(apa + mn_chunk(64 + r0, cl), kx.get());
+                        if (!sub) {
+                            sts16(apb + mn_chunk(r0, cl), dq.get());
+                            sts16(apb + mn_chunk(64 + r0, cl), dk.get());
+                            sts16(apa + mn_chunk(r0, cl), dd.get());
+                        }
+                    }
+                    Q *= al[i];
                 }
-            }
-        }
-        {   // backward: kappa (Kbar to the record); half 0 also xi = exp(g_47 - g_s)
-            float Q = 1.f;
-            float kb[8], kx[8];
-#pragma unroll
-            for (int i = 31; i >= 0; --i) {
-                const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-                kb[i & 7] = kf * (hh ? Q : Q * H1);
-                kx[i & 7] = kf * (Q * mid);
-                if ((i & 7) == 0) {
-                    sts16(qk_stage + 16384 + row64_chunk_off(c, (32 * hh + i) >> 3), pack8(kb));
-                    if (!hh) sts16(apa + mn_chunk(64 + i, c), pack8(kx));
-                }
-                Q *= al[i];
-            }
-        }
-        {   // backward to the half's reference token: phi = 1/D, psi = D (local tokens 0..15)
-            float Dd = 1.f;
-            float dq[8], dk[8], dd[8];
-#pragma unroll
-            for (int i = 15; i >= 0; --i) {
-                const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
-                const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-                guard_bad |= !(Dd >= kGuardMin);
-                const float inv = __fdividef(1.f, Dd);
-                dq[i & 7] = qf * inv;
-                dk[i & 7] = kf * inv;
-                dd[i & 7] = kf * Dd;
-                if ((i & 7) == 0) {
-                    const uint32_t r0 = 32 * hh + i;
-                    sts16(apb + mn_chunk(r0, c), pack8(dq));
-                    sts16(apb + mn_chunk(64 + r0, c), pack8(dk));
-                    sts16(apa + mn_chunk(r0, c), pack8(dd));
-                }
-                Dd *= al[i];
             }
         }
         if (guard_bad) atomicOr(&ms.guard_fail, 1);
@@ -409,22 +417,21 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         fence_after_sync();
 
         if (tid == 0) {
-            bulk_s2g(rec + kRecQ, S + kSal, 32768);     // Q~ and Kbar are adjacent in the record
-            bulk_commit();
             if (ms.guard_fail) {
                 atomicOr(&p.chain_flag[(int64_t)it.seq * H + it.h], 1);
                 ms.guard_fail = 0;
             }
             const uint32_t idesc = idesc_bf16(128, 128, true, true);
 #pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks)
-                mma_bf16(tbase, sdesc(apa + ks * 2 * kSbo, kLbo, kSbo), sdesc(apb + ks * 2 * kSbo, kLbo, kSbo), idesc,
-                         ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < kD / 16; ++ks) {
+                const uint32_t R = s_base + (ks >> 2) * kRound + (ks & 3) * 2 * kSbo;
+                mma_bf16(tbase, sdesc(R + kRa, kLbo, kSbo), sdesc(R + kRb, kLbo, kSbo), idesc, ks > 0 ? 1u : 0u);
+            }
             mma_commit(&ms.bar_mma);
-            mma_issued += 1;
+            ms.mma_issued += 1;
         }
         ok = mbar_wait(&ms.bar_mma, 0);
-        if (tid == 0 && ok) mma_waited += 1;
+        if (tid == 0 && ok) ms.mma_waited += 1;
         if (__syncthreads_or(!ok)) {
             ok = false;
             break;
@@ -486,9 +493,10 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         // ------------------------------------------------------------ phase 3: T
         invert_unit_lower(reinterpret_cast<const float*>(sm + kAmat), reinterpret_cast<float*>(sm + kTf),
                           reinterpret_cast<float*>(sm + kTscr), tid);
-        {   // T^T row s (= column s of T, zero above the diagonal) as the MN-major [s][r] operand
+        {   // T'^T row s = beta_s (column s of T, zero above the diagonal), the MN-major [s][r] operand
             const float* Tf = reinterpret_cast<const float*>(sm + kTf);
             const int srow = tid >> 2;
+            const float bs = bsm[srow];
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
                 const int cc = 2 * (tid & 3) + q2;
@@ -496,7 +504,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int r = 8 * cc + e;
-                    x[e] = r >= srow ? Tf[r * kC + srow] : 0.f;
+                    x[e] = r >= srow ? Tf[r * kC + srow] * bs : 0.f;
                 }
                 sts16(s_base + kTm + row64_chunk_off(srow, cc), pack8(x));
             }
@@ -507,30 +515,28 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         fence_after_sync();
 
         if (tid == 0) {
-            const uint32_t idesc = idesc_bf16(128, 64, false, true);
+            // W^T = X^T T'^T (X^T K-major); U~^T = V^T T'^T with V^T the swizzled
+            // v tile read MN-major (64-channel blocks 8 KiB apart, 8-token groups 1 KiB apart)
+            const uint32_t idesc_k = idesc_bf16(128, 64, false, true);
+            const uint32_t idesc_mn = idesc_bf16(128, 64, true, true);
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tbase, sdesc(Ss + kSq + ks * 32, 16, 1024), sdesc(s_base + kTm + ks * 2048, 1024, 1024),
-                         idesc, ks > 0 ? 1u : 0u);
+                mma_bf16(tbase, sdesc(s_base + kX + ks * 32, 16, 1024), sdesc(s_base + kTm + ks * 2048, 1024, 1024),
+                         idesc_k, ks > 0 ? 1u : 0u);
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tbase + 64, sdesc(Ss + kSv + ks * 32, 16, 1024), sdesc(s_base + kTm + ks * 2048, 1024, 1024),
-                         idesc, ks > 0 ? 1u : 0u);
+                mma_bf16(tbase + 64, sdesc(s_base + kSv + ks * 2048, kVbox, 1024),
+                         sdesc(s_base + kTm + ks * 2048, 1024, 1024), idesc_mn, ks > 0 ? 1u : 0u);
             mma_commit(&ms.bar_mma);
-            mma_issued += 1;
+            ms.mma_issued += 1;
         }
         ok = mbar_wait(&ms.bar_mma, 1);
-        if (tid == 0 && ok) mma_waited += 1;
+        if (tid == 0 && ok) ms.mma_waited += 1;
         if (__syncthreads_or(!ok)) {
             ok = false;
             break;
         }
         fence_after_sync();
-        // this stage is no longer read: fetch the item two steps ahead into it
-        if (tid == 0 && item + 2 * step < n_items) {
-            bulk_wait_read();                          // the staged Q~ / Kbar left this stage
-            issue_load(item + 2 * step, info_nxt2, st);
-        }
 
         // ------------------------------------------------------------ phase 4: W and U~ to the record
         {
@@ -552,10 +558,6 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             }
         }
         // beta of the next item into its buffer; start loading the one after
-        if (tid < kC) ms.beta[st ^ 1][tid] = beta_next;
-        beta_next = load_beta(item + 2 * step, info_nxt2);
-        info_cur = info_nxt;
-        info_nxt = info_nxt2;
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -564,6 +566,11 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             bulk_s2g(rec + kRecW, sm + kWst, 16384);
             bulk_s2g(rec + kRecU, sm + kWst + 16384, 16384);
             bulk_commit();
+            // the next item's tiles land where P, W and U~ are staged
+            if (item + step < n_items) {
+                bulk_wait_read();
+                issue_load(item + step, item_info(p, item + step, n_items));
+            }
         }
     }
 
@@ -572,9 +579,8 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         // let this CTA's own copies and MMAs in flight land (bounded) before
         // shared and tensor memory are released
         flag(p.status, KDA_DEV_WAIT_TIMEOUT);
-        for (int st = 0; st < 2; ++st)
-            for (uint32_t l = ld_waited[st]; l < ld_issued[st]; ++l) mbar_wait(&ms.bar_load[st], l & 1);
-        for (uint32_t m = mma_waited; m < mma_issued; ++m) mbar_wait(&ms.bar_mma, m & 1);
+        for (uint32_t l = ms.ld_waited; l < ms.ld_issued; ++l) mbar_wait(&ms.bar_load, l & 1);
+        for (uint32_t m = ms.mma_waited; m < ms.mma_issued; ++m) mbar_wait(&ms.bar_mma, m & 1);
     }
     fence_before_sync();
     __syncthreads();
@@ -681,18 +687,19 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [rows x cols] row-major tensor, boxes of 64 rows x 128 elements, no swizzle;
-// rows past the end read as zero.
+// [rows x cols] row-major tensor, boxes of 64 rows x box_cols elements, with or
+// without the 128-byte swizzle; rows past the end read as zero.  Every box here
+// starts at a column that is a multiple of 64, a multiple of 16 bytes.
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* base, int64_t rows,
-              int64_t cols) {
+              int64_t cols, uint32_t box_cols, CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
-    const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)kC};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kC};
     const cuuint32_t es[2] = {1, 1};
     return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -703,10 +710,11 @@ cudaError_t launch_chunk_local(const ChunkLaunch& p, cudaStream_t s) {
     if (max_items == 0 || p.a.total_tokens == 0) return cudaSuccess;
     LocalMaps tm;
     const int64_t rows = p.a.total_tokens, cols = (int64_t)p.a.n_heads * kD;
-    if (!make_map(&tm.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a.q, rows, cols) ||
-        !make_map(&tm.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a.k, rows, cols) ||
-        !make_map(&tm.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a.v, rows, cols) ||
-        !make_map(&tm.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.a.alpha, rows, cols))
+    const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE, sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_map(&tm.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a.q, rows, cols, 64, none) ||
+        !make_map(&tm.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a.k, rows, cols, 64, none) ||
+        !make_map(&tm.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.a.v, rows, cols, 64, sw128) ||
+        !make_map(&tm.alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.a.alpha, rows, cols, 64, none))
         return cudaErrorInvalidValue;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -715,7 +723,11 @@ cudaError_t launch_chunk_local(const ChunkLaunch& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(chunk_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t grid = max_items < sms ? max_items : sms;
+    e = cudaFuncSetAttribute(chunk_local_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = (int64_t)kCtasPerSm * sms;
+    const int64_t grid = max_items < slots ? max_items : slots;
     note_launch();
     chunk_local_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(p, tm);
     return cudaGetLastError();
