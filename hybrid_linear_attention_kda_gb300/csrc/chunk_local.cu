@@ -304,8 +304,12 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         // beta of this item (first read after the A/P MMA, several barriers on)
         if (tid < kC) ms.beta[tid] = tid < n ? a.beta[(it.t0 + tid) * H + it.h] : 0.f;
 
-        ok = mbar_wait(&ms.bar_load, (uint32_t)(k & 1));
-        if (tid == 0 && ok) ms.ld_waited += 1;
+        // thread 0 alone polls the mbarrier; the others wait at the CTA barrier,
+        // which takes no issue slots from the co-resident CTA
+        if (tid == 0) {
+            ok = mbar_wait(&ms.bar_load, (uint32_t)(k & 1));
+            if (ok) ms.ld_waited += 1;
+        }
         if (__syncthreads_or(!ok)) {
             ok = false;
             break;
@@ -350,9 +354,9 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             const float xi_rest = qq == 0 ? Q1 * Q2 : Q2;      // tokens after the quarter, up to 47
             if (qq == 0) reinterpret_cast<float*>(rec + kRecG)[c] = (Q0 * Q1) * (Q2 * Q3);
             const uint32_t apa = Rs + kRa, apb = Rs + kRb;
-            {   // forward: Gamma -> Q~ (record), X^T = Gamma k; in sub 1 also phi, psi
+            {   // forward: Gamma -> Q~ (record), X^T = Gamma k
                 float P = 1.f;
-                Pack8 gq, xk, dq, dk, dd;
+                Pack8 gq, xk;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
@@ -361,52 +365,69 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
                     const float G = before * P;
                     gq.put(i & 7, qf * G);
                     xk.put(i & 7, kf * G);
-                    if (sub) {
-                        guard_bad |= !(P >= kGuardMin);
-                        const float inv = __fdividef(1.f, P);
-                        dq.put(i & 7, qf * P);
-                        dk.put(i & 7, kf * P);
-                        dd.put(i & 7, kf * inv);
-                    }
                     if ((i & 7) == 7) {
                         const uint32_t r0 = r_base + (i & ~7);
                         stg16(rec + kRecQ + row64_chunk_off(c, r0 >> 3), gq.get());
                         sts16(s_base + kX + row64_chunk_off(c, r0 >> 3), xk.get());
-                        if (sub) {
-                            sts16(apb + mn_chunk(r0, cl), dq.get());
-                            sts16(apb + mn_chunk(64 + r0, cl), dk.get());
-                            sts16(apa + mn_chunk(r0, cl), dd.get());
-                        }
                     }
                 }
             }
-            {   // backward: kappa -> Kbar (record); half 0 also xi; in sub 0 also phi, psi
+            if (sub) {   // up from the half's reference token: phi = E, psi = 1/E
+                float E = 1.f;
+                Pack8 dq, dk, dd;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
+                    const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+                    E *= al[i];
+                    guard_bad |= !(E >= kGuardMin);
+                    const float inv = __fdividef(1.f, E);
+                    dq.put(i & 7, qf * E);
+                    dk.put(i & 7, kf * E);
+                    dd.put(i & 7, kf * inv);
+                    if ((i & 7) == 7) {
+                        const uint32_t r0 = r_base + (i & ~7);
+                        sts16(apb + mn_chunk(r0, cl), dq.get());
+                        sts16(apb + mn_chunk(64 + r0, cl), dk.get());
+                        sts16(apa + mn_chunk(r0, cl), dd.get());
+                    }
+                }
+            }
+            {   // backward: kappa -> Kbar (record); half 0 also xi
                 float Q = 1.f;
-                Pack8Rev kb, kx, dq, dk, dd;
+                Pack8Rev kb, kx;
 #pragma unroll
                 for (int i = 15; i >= 0; --i) {
-                    const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
                     const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
                     kb.put(i & 7, kf * (Q * after));
                     if (!hh) kx.put(i & 7, kf * (Q * xi_rest));
-                    if (!sub) {
-                        guard_bad |= !(Q >= kGuardMin);
-                        const float inv = __fdividef(1.f, Q);
-                        dq.put(i & 7, qf * inv);
-                        dk.put(i & 7, kf * inv);
-                        dd.put(i & 7, kf * Q);
-                    }
                     if ((i & 7) == 0) {
                         const uint32_t r0 = r_base + i;
                         stg16(rec + kRecK + row64_chunk_off(c, r0 >> 3), kb.get());
                         if (!hh) sts16(apa + mn_chunk(64 + r0, cl), kx.get());
-                        if (!sub) {
-                            sts16(apb + mn_chunk(r0, cl), dq.get());
-                            sts16(apb + mn_chunk(64 + r0, cl), dk.get());
-                            sts16(apa + mn_chunk(r0, cl), dd.get());
-                        }
                     }
                     Q *= al[i];
+                }
+            }
+            if (!sub) {  // down to the half's reference token: phi = 1/D, psi = D
+                float D = 1.f;
+                Pack8Rev dq, dk, dd;
+#pragma unroll
+                for (int i = 15; i >= 0; --i) {
+                    const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
+                    const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
+                    guard_bad |= !(D >= kGuardMin);
+                    const float inv = __fdividef(1.f, D);
+                    dq.put(i & 7, qf * inv);
+                    dk.put(i & 7, kf * inv);
+                    dd.put(i & 7, kf * D);
+                    if ((i & 7) == 0) {
+                        const uint32_t r0 = r_base + i;
+                        sts16(apb + mn_chunk(r0, cl), dq.get());
+                        sts16(apb + mn_chunk(64 + r0, cl), dk.get());
+                        sts16(apa + mn_chunk(r0, cl), dd.get());
+                    }
+                    D *= al[i];
                 }
             }
         }
@@ -430,8 +451,10 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             mma_commit(&ms.bar_mma);
             ms.mma_issued += 1;
         }
-        ok = mbar_wait(&ms.bar_mma, 0);
-        if (tid == 0 && ok) ms.mma_waited += 1;
+        if (tid == 0) {
+            ok = mbar_wait(&ms.bar_mma, 0);
+            if (ok) ms.mma_waited += 1;
+        }
         if (__syncthreads_or(!ok)) {
             ok = false;
             break;
@@ -530,8 +553,10 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             mma_commit(&ms.bar_mma);
             ms.mma_issued += 1;
         }
-        ok = mbar_wait(&ms.bar_mma, 1);
-        if (tid == 0 && ok) ms.mma_waited += 1;
+        if (tid == 0) {
+            ok = mbar_wait(&ms.bar_mma, 1);
+            if (ok) ms.mma_waited += 1;
+        }
         if (__syncthreads_or(!ok)) {
             ok = false;
             break;
