@@ -34,7 +34,8 @@ constexpr uint32_t kStage0 = 49152;
 constexpr uint32_t kStageStride = 74752;  // kRecBytes rounded up to 1024
 constexpr uint32_t kMisc = kStage0 + 2 * kStageStride;
 constexpr size_t kSmemBytes = kMisc + 128 + 1024;
-constexpr uint32_t kTmemCols = 512;       // [D1 | D2] x 2 at [0,128) and [128,256), D3 [256,384)
+constexpr uint32_t kTmemCols = 512;       // [D1 | D2] x 2 at [0,128) and [128,256), D3 [256,384),
+                                          // snapshot staging [384,512)
 
 struct Misc {
     uint64_t bar_load[2];   // record copies (tx bytes)
@@ -44,9 +45,13 @@ struct Misc {
     uint64_t bar_u;         // state group: U^T written            (256 arrivals)
     uint64_t bar_s;         // state group: bf16 S^T written        (256 arrivals)
     uint64_t bar_o;         // output group: D2 read from TMEM     (128 arrivals)
+    uint64_t bar_snap;      // state group: snapshot staged in TMEM (256 arrivals)
+    uint64_t bar_snapfree;  // output group: staged snapshot written out (128 arrivals)
     uint32_t tslot;
     int32_t failed;
 };
+
+static_assert(sizeof(Misc) <= 128, "barrier block");
 
 __device__ __forceinline__ void sts16(uint32_t saddr, uint4 v) { st_shared_v4(saddr, v.x, v.y, v.z, v.w); }
 
@@ -82,6 +87,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         mbar_init(&ms.bar_u, 32 * kStateWarps);
         mbar_init(&ms.bar_s, 32 * kStateWarps);
         mbar_init(&ms.bar_o, 32 * kOutWarps);
+        mbar_init(&ms.bar_snap, 32 * kStateWarps);
+        mbar_init(&ms.bar_snapfree, 32 * kOutWarps);
         ms.failed = 0;
         fence_mbar_init();
     }
@@ -90,6 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     fence_after_sync();
     const uint32_t tbase = ms.tslot;
     const uint32_t tD3 = tbase + 256;
+    const uint32_t tSnap = tbase + 384;       // S^T [j][c] of the latest snapshot
     // [D1 | D2] of chunk lc: one N = 128 accumulator, double-buffered
     auto tD1 = [&](int64_t lc) -> uint32_t { return tbase + 128 * (uint32_t)(lc & 1); };
     auto tD2 = [&](int64_t lc) -> uint32_t { return tbase + 128 * (uint32_t)(lc & 1) + 64; };
@@ -99,6 +107,25 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         if (mbar_wait(bar, parity)) return true;
         atomicExch(&ms.failed, 1);
         return false;
+    };
+
+    // pool slot of the snapshot after chunk lc, or -1 (none, skipped, or a bad
+    // index, which `report` flags)
+    auto snap_slot = [&](int64_t lc, bool report) -> int32_t {
+        if (!a.snap_table) return -1;
+        const int64_t t0 = tb + lc * kC;
+        const int n = (int)(te - t0 < kC ? te - t0 : kC);
+        const int64_t p_end = pos0 + lc * kC + n;
+        if (p_end % a.snap_interval != 0) return -1;
+        const int64_t ord = p_end / a.snap_interval - 1;
+        if (ord >= a.snap_table_stride) {
+            if (report) flag(p.status, KDA_DEV_BAD_ORDINAL);
+            return -1;
+        }
+        const int32_t slot = a.snap_table[(int64_t)seq * a.snap_table_stride + ord];
+        if (slot >= 0 && (int64_t)slot < a.n_slots) return slot;
+        if (slot != -1 && report) flag(p.status, KDA_DEV_BAD_SLOT);
+        return -1;
     };
 
     if (warp == kIssuerWarp) {
@@ -216,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         };
         write_sa();
         bool ok = true;
+        uint32_t n_snap = 0;
         for (int64_t lc = 0; lc < nc; ++lc) {
             const uint32_t par = (uint32_t)(lc & 1);
             const uint8_t* stage_p = sm + stage_of(lc);
@@ -260,24 +288,23 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
             }
             fence_before_sync();
             write_sa();
-            // snapshot after this chunk, straight from the fp32 registers
-            const int64_t t0 = tb + lc * kC;
-            const int n = (int)(te - t0 < kC ? te - t0 : kC);
-            const int64_t p_end = pos0 + lc * kC + n;
-            if (a.snap_table && p_end % a.snap_interval == 0) {
-                const int64_t ord = p_end / a.snap_interval - 1;
-                if (ord >= a.snap_table_stride) {
-                    if (tid == 0) flag(p.status, KDA_DEV_BAD_ORDINAL);
-                } else {
-                    const int32_t slot = a.snap_table[(int64_t)seq * a.snap_table_stride + ord];
-                    if (slot >= 0 && (int64_t)slot < a.n_slots) {
-                        float* dst = a.pool + (int64_t)slot * slot_stride + head_off;
+            // snapshot after this chunk: the fp32 state goes to the snapshot
+            // columns of TMEM (lane j, column c); the output group writes it to
+            // the pool, off this chain
+            if (snap_slot(lc, tid == 0) >= 0) {
+                if (n_snap > 0 && !(ok = waitb(&ms.bar_snapfree, (n_snap - 1) & 1))) break;
+                fence_after_sync();
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
-                    } else if (slot != -1 && tid == 0) {
-                        flag(p.status, KDA_DEV_BAD_SLOT);
-                    }
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(S[16 * q4 + e]);
+                    tmem_st16(tSnap + lanebase + cbase + 16 * q4, v);
                 }
+                tmem_wait_st();
+                fence_before_sync();
+                mbar_arrive(&ms.bar_snap);
+                n_snap += 1;
             }
         }
         if (ok && a.final_state) {
@@ -292,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         const uint32_t lanebase = (uint32_t)(32 * jq) << 16;
         __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
         const int64_t ostride = (int64_t)H * kD;
+        uint32_t n_snap = 0;
         for (int64_t lc = 0; lc < nc; ++lc) {
             if (!waitb(&ms.bar_c, (uint32_t)(lc & 1))) break;
             fence_after_sync();
@@ -310,6 +338,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
                 for (int e = 0; e < 16; ++e)
                     if (16 * q4 + e < n)
                         orow[(16 * q4 + e) * ostride] = __float2bfloat16_rn(a.scale * __uint_as_float(v[q4][e]));
+            }
+            // a snapshot after this chunk: from the TMEM staging to the pool's [c][j] layout
+            const int32_t slot = snap_slot(lc, false);
+            if (slot >= 0) {
+                if (!waitb(&ms.bar_snap, n_snap & 1)) break;
+                fence_after_sync();
+                float* dst = a.pool + (int64_t)slot * slot_stride + head_off + j;
+#pragma unroll 2
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t sv[16];
+                    tmem_ld16(tSnap + lanebase + 16 * q, sv);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) dst[(int64_t)(16 * q + e) * kD] = __uint_as_float(sv[e]);
+                }
+                fence_before_sync();
+                mbar_arrive(&ms.bar_snapfree);
+                n_snap += 1;
             }
         }
     }
