@@ -58,12 +58,14 @@ constexpr uint32_t kTf = 16384;            // T fp32 [64][64]
 constexpr uint32_t kTscr = 32768;          // block-product scratch, 1024 fp32
 constexpr uint32_t kTm = 36864;            // (T diag(beta))^T bf16, MN-major [s][r]
 constexpr uint32_t kPst = 45056;           // P record tile, staged for its bulk store
-constexpr uint32_t kWst = 0;               // after the W/U~ MMA: W and U~ record tiles, staged
+constexpr uint32_t kWst = kSv;             // after the W/U~ MMA: W and U~ record tiles, staged
+                                           // over v and X^T, so the next item's q, k, alpha can land
 constexpr uint32_t kMisc = 98304;
 constexpr uint32_t kTmemCols = 128;
 
 struct Misc {
-    float beta[kC];
+    float beta[2][kC];         // this item's and the next item's beta
+    int4 info[2];              // this item's and the next item's chunk-table entry
     float qprod[2][4][64];     // per round: product of alpha over each 16-token quarter, per channel
     uint64_t bar_load;
     uint64_t bar_mma;
@@ -262,7 +264,9 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         fence_mbar_init();
     }
     // thread 0 issues every copy and MMA and counts them, to drain on a timeout
-    auto issue_load = [&](int64_t item, int4 info) {
+    // an item's q, k and alpha (with the whole 80 KiB expected on the barrier),
+    // then, once the staging above them has been read, its v
+    auto issue_load_qka = [&](int64_t item, int4 info) {
         const Item it = decode_item(p, item, info);
         mbar_expect_tx(&ms.bar_load, kLoadBytes);
         const int32_t x = it.h * kD, y = (int32_t)it.t0;
@@ -272,9 +276,14 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             tma_load_2d(R + kRq, &tm.q, x + 64 * g, y, &ms.bar_load);
             tma_load_2d(R + kRk, &tm.k, x + 64 * g, y, &ms.bar_load);
             tma_load_2d(R + kRal, &tm.alpha, x + 64 * g, y, &ms.bar_load);
-            tma_load_2d(sm + kSv + g * kVbox, &tm.v, x + 64 * g, y, &ms.bar_load);
         }
         ms.ld_issued += 1;
+    };
+    auto issue_load_v = [&](int64_t item, int4 info) {
+        const Item it = decode_item(p, item, info);
+        const int32_t x = it.h * kD, y = (int32_t)it.t0;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) tma_load_2d(sm + kSv + g * kVbox, &tm.v, x + 64 * g, y, &ms.bar_load);
     };
     fence_before_sync();
     __syncthreads();
@@ -286,8 +295,17 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm.v)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm.alpha)) : "memory");
     }
-    if (tid == 0) issue_load(first, item_info(p, first, n_items));
+    if (tid == 0) {
+        const int4 info0 = item_info(p, first, n_items);
+        ms.info[0] = info0;
+        issue_load_qka(first, info0);
+        issue_load_v(first, info0);
+    }
     __syncthreads();
+    if (tid < kC) {
+        const Item it0 = decode_item(p, first, ms.info[0]);
+        ms.beta[0][tid] = tid < it0.n ? a.beta[(it0.t0 + tid) * H + it0.h] : 0.f;
+    }
 
     const int cl = tid & 63;       // channel within a round
     const int qq = tid >> 6;       // which 16-token quarter of the chunk this thread walks
@@ -297,12 +315,13 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
     bool ok = true;
     int k = 0;
     for (int64_t item = first; item < n_items; item += step, ++k) {
-        const Item it = decode_item(p, item, item_info(p, item, n_items));
+        const int nb = (k + 1) & 1;             // the next item's buffers
+        const Item it = decode_item(p, item, ms.info[k & 1]);
         const int n = it.n;
         uint8_t* rec = p.records + ((size_t)it.g * H + it.h) * kRecBytes;
-        const float* bsm = ms.beta;
-        // beta of this item (first read after the A/P MMA, several barriers on)
-        if (tid < kC) ms.beta[tid] = tid < n ? a.beta[(it.t0 + tid) * H + it.h] : 0.f;
+        const float* bsm = ms.beta[k & 1];
+        // the next item's chunk-table entry (thread 0; read after later barriers)
+        if (tid == 0) ms.info[nb] = item_info(p, item + step, n_items);
 
         // thread 0 alone polls the mbarrier; the others wait at the CTA barrier,
         // which takes no issue slots from the co-resident CTA
@@ -513,6 +532,13 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             bulk_commit();
         }
 
+        // the next item's beta: loaded now, stored after phase 4, so the global
+        // load's latency passes while T is inverted
+        float beta_nx = 0.f;
+        if (tid < kC && item + step < n_items) {
+            const Item nx = decode_item(p, item + step, ms.info[nb]);
+            if (tid < nx.n) beta_nx = a.beta[(nx.t0 + tid) * H + nx.h];
+        }
         // ------------------------------------------------------------ phase 3: T
         invert_unit_lower(reinterpret_cast<const float*>(sm + kAmat), reinterpret_cast<float*>(sm + kTf),
                           reinterpret_cast<float*>(sm + kTscr), tid);
@@ -562,6 +588,12 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             break;
         }
         fence_after_sync();
+        // [0, 64 KiB) is free once the staged P has been read: the next item's
+        // q, k and alpha go there now
+        if (tid == 0 && item + step < n_items) {
+            bulk_wait_read();
+            issue_load_qka(item + step, ms.info[nb]);
+        }
 
         // ------------------------------------------------------------ phase 4: W and U~ to the record
         {
@@ -582,7 +614,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
                 }
             }
         }
-        // beta of the next item into its buffer; start loading the one after
+        if (tid < kC) ms.beta[nb][tid] = beta_nx;
         fence_async_smem();
         fence_before_sync();
         __syncthreads();
@@ -591,10 +623,10 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             bulk_s2g(rec + kRecW, sm + kWst, 16384);
             bulk_s2g(rec + kRecU, sm + kWst + 16384, 16384);
             bulk_commit();
-            // the next item's tiles land where P, W and U~ are staged
+            // the next item's v lands where W and U~ are staged
             if (item + step < n_items) {
                 bulk_wait_read();
-                issue_load(item + step, item_info(p, item + step, n_items));
+                issue_load_v(item + step, ms.info[nb]);
             }
         }
     }
