@@ -22,6 +22,10 @@ Contents
                    the prefix-cache policy: chained 256-token hashes, interval
                    retention, second-hit admission, next-step reuse
                    ("Kimi K3 Tech Intro", sections 2.2-2.4 and 3).
+``verify_steps`` / ``commit_steps``
+                   a speculative decoding step: T candidate tokens run without
+                   touching the state (outputs and update vectors), then the
+                   accepted ones applied ("Kimi K3 Tech Intro", section 6).
 ``window_bound``   a rigorous upper bound on how much a state that is forgotten
                    at the start of a window can change the states inside it,
                    used to check long sequences on sampled windows.
@@ -31,3 +35,4 @@ from .chunked import chunked  # noqa: F401
 from .positions import snapshot_positions, reusable_prefix  # noqa: F401
 from .bounds import window_bound, state_norm_bound  # noqa: F401
 from .prefix_cache import PrefixCacheIndex, block_hashes  # noqa: F401
+from .speculative import verify_steps, commit_steps  # noqa: F401
