@@ -387,6 +387,48 @@ def bench_ours(args, rank, world, dev, dist_on):
     barrier(dist_on)
     dec_e2e_ms = max_over_ranks(d0.elapsed_time(d1), dist_on, dev) / args.steps
 
+    # ---- speculative decoding: 8 candidates per sequence verified, 5 accepted
+    # (the pages' low-entropy average is 4.73 accepted tokens per step)
+    sT, s_acc = 8, 5
+    sins = [{k_: t.to(dev).reshape((dn, sT) + tuple(t.shape[1:]))
+             for k_, t in inputs.gen_decode(dn * sT, dH, dd, dd, dw["seed"], 200 + s).items()} for s in range(2)]
+    so = torch.empty((dn, sT, dH, dd), dtype=torch.bfloat16, device=dev)
+    su = torch.empty((dn, sT, dH, dd), dtype=torch.float32, device=dev)
+    sacc = torch.full((dn,), s_acc, dtype=torch.int32, device=dev)
+
+    def spec_once(i, part):
+        z = sins[i % 2]
+        if part in ("verify", "both"):
+            kda.kda_decode_verify(z["q"], z["k"], z["v"], z["alpha"], z["beta"], dpool, dslots, so, su,
+                                  stream=stream)
+        if part in ("commit", "both"):
+            kda.kda_decode_commit(z["k"], z["alpha"], su, sacc, dpool, dslots, stream=stream)
+
+    spec_ms = {}
+    for part in ("verify", "commit", "both"):
+        for i in range(warm):
+            spec_once(i, part)
+        barrier(dist_on)
+        d0.record(stream)
+        for i in range(args.steps):
+            spec_once(i, part)
+        d1.record(stream)
+        barrier(dist_on)
+        spec_ms[part] = max_over_ranks(d0.elapsed_time(d1), dist_on, dev) / args.steps
+    assert kda.kda_check_status(stream) == 0
+    st_bytes = dn * dH * dd * dd * 4
+    tok_in = dn * sT * dH * (3 * dd * 2 + dd * 4 + 4)          # q, k, v bf16, alpha, beta
+    ver_bytes = st_bytes + tok_in + dn * sT * dH * dd * (2 + 4)  # + o bf16, u fp32
+    com_bytes = 2 * st_bytes + dn * s_acc * dH * dd * (2 + 4 + 4)  # + k, alpha, u of accepted tokens
+    spec = {"workload": f"{dn} sequences x {dH} heads, d={dd}, {sT} candidate tokens verified and "
+                        f"{s_acc} accepted per step",
+            "value": dn * s_acc / (spec_ms["both"] / 1e3), "unit": "accepted tokens/s",
+            "ms_per_step": spec_ms["both"], "verify_ms": spec_ms["verify"], "commit_ms": spec_ms["commit"],
+            "verify_gbs": ver_bytes / (spec_ms["verify"] / 1e3) / 1e9,
+            "commit_gbs": com_bytes / (spec_ms["commit"] / 1e3) / 1e9,
+            "state_bytes_per_accepted_token": 3 * dd * dd * 4 / s_acc,
+            "decode_state_bytes_per_token": 2 * dd * dd * 4}
+
     # ---- snapshot gather + restore of 128 states (64 KiB each)
     gsl = torch.arange(0, 2 * 128, 2, dtype=torch.int32, device=dev) % dn
     gbuf = torch.empty((128, dH, dd, dd), dtype=torch.float32, device=dev)
@@ -433,6 +475,7 @@ def bench_ours(args, rank, world, dev, dist_on):
                    "e2e": {"value": world * dbytes / (dec_e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                            "ms_per_step": dec_e2e_ms, "h2d_bytes_per_step": d_h2d,
                            "d2h_bytes_per_step": d_d2h}},
+        "speculative_decode": spec,
         "snapshot_copy": {"value": copy_bytes / (copy_ms / 1e3) / 1e9, "unit": "GB/s",
                           "ms_per_step": copy_ms, "states": 128},
         "kernel_fingerprint": fp,

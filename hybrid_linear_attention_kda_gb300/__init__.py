@@ -20,6 +20,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_DEVICE_S
     KDA_ERR_TIMEOUT, KDA_ERR_NO_MEMORY = range(7)
 KDA_BF16, KDA_FP32 = 0, 1
 KDA_DEV_BAD_SLOT, KDA_DEV_BAD_START, KDA_DEV_BAD_SEQLENS, KDA_DEV_BAD_ORDINAL = 0x1, 0x2, 0x4, 0x8
+KDA_DEV_WAIT_TIMEOUT, KDA_DEV_BAD_ACCEPT = 0x10, 0x20
 
 CHUNK = 64
 SNAP_INTERVAL = 256
@@ -82,6 +83,10 @@ def load():
                                                ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_char_p)]
     lib.kda_decode_step.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, vp, f32, vp]
+    lib.kda_decode_verify.restype = ctypes.c_int
+    lib.kda_decode_verify.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, f32, vp]
+    lib.kda_decode_commit.restype = ctypes.c_int
+    lib.kda_decode_commit.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, i64, vp, vp]
     lib.kda_snapshot_gather.restype = ctypes.c_int
     lib.kda_snapshot_gather.argtypes = [vp, i64, vp, i32, i32, i32, i32, vp, vp]
     lib.kda_snapshot_restore.restype = ctypes.c_int
@@ -200,6 +205,25 @@ def kda_decode_step(q, k, v, alpha, beta, pool, state_slot, o, scale=1.0, stream
     _check(load().kda_decode_step(n, H, d_k, d_v, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
                                   _ptr(alpha), _ptr(beta), _ptr(pool), pool.shape[0],
                                   _ptr(state_slot), _ptr(o), float(scale), _stream_handle(stream)))
+
+
+def kda_decode_verify(q, k, v, alpha, beta, pool, state_slot, o, u, scale=1.0, stream=None):
+    """Run T candidate tokens per sequence without touching the states:
+    q, k, alpha [n, T, H, d_k]; v, o, u [n, T, H, d_v]; beta [n, T, H]."""
+    n, T, H, d_k = q.shape
+    d_v = v.shape[3]
+    _check(load().kda_decode_verify(n, T, H, d_k, d_v, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
+                                    _ptr(alpha), _ptr(beta), _ptr(pool), pool.shape[0], _ptr(state_slot),
+                                    _ptr(o), _ptr(u), float(scale), _stream_handle(stream)))
+
+
+def kda_decode_commit(k, alpha, u, n_accept, pool, state_slot, stream=None):
+    """Apply the first n_accept[i] verified updates of sequence i to its state."""
+    n, T, H, d_k = k.shape
+    d_v = u.shape[3]
+    _check(load().kda_decode_commit(n, T, H, d_k, d_v, _dtype_code(k), _ptr(k), _ptr(alpha), _ptr(u),
+                                    _ptr(n_accept), _ptr(pool), pool.shape[0], _ptr(state_slot),
+                                    _stream_handle(stream)))
 
 
 def kda_snapshot_gather(pool, slots, dst, stream=None):

@@ -304,6 +304,67 @@ kda_status_t kda_decode_step(int32_t n_seqs, int32_t n_heads, int32_t d_k, int32
     return KDA_OK;
 }
 
+static kda_status_t check_spec(int32_t n_seqs, int32_t n_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
+                               int32_t dtype, int64_t n_slots) {
+    kda_status_t st = check_dims(n_heads, d_k, d_v, dtype);
+    if (st != KDA_OK) return st;
+    if (n_tokens < 1 || n_tokens > 16) return fail(KDA_ERR_UNSUPPORTED, "n_tokens must be in [1, 16] (got %d)", n_tokens);
+    if (n_seqs < 0 || n_seqs > kMaxSeqs) return fail(KDA_ERR_INVALID_ARG, "n_seqs %d", n_seqs);
+    if (n_slots < 0) return fail(KDA_ERR_INVALID_ARG, "n_slots < 0");
+    if ((int64_t)n_seqs * n_heads > (int64_t)INT32_MAX) return fail(KDA_ERR_INVALID_ARG, "n_seqs * n_heads too large");
+    return KDA_OK;
+}
+
+kda_status_t kda_decode_verify(int32_t n_seqs, int32_t n_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
+                               int32_t dtype, const void* q, const void* k, const void* v,
+                               const float* alpha, const float* beta, const float* pool,
+                               int64_t n_slots, const int32_t* state_slot, void* o, float* u,
+                               float scale, void* stream) {
+    kda_status_t st = check_spec(n_seqs, n_tokens, n_heads, d_k, d_v, dtype, n_slots);
+    if (st != KDA_OK) return st;
+    if (n_seqs == 0) return KDA_OK;
+    KDA_REQUIRE_PTR(q, "q");
+    KDA_REQUIRE_PTR(k, "k");
+    KDA_REQUIRE_PTR(v, "v");
+    KDA_REQUIRE_PTR(alpha, "alpha");
+    KDA_REQUIRE_PTR(beta, "beta");
+    KDA_REQUIRE_PTR(pool, "pool");
+    KDA_REQUIRE_PTR(state_slot, "state_slot");
+    KDA_REQUIRE_PTR(o, "o");
+    KDA_REQUIRE_PTR(u, "u");
+    if (n_slots == 0) return fail(KDA_ERR_INVALID_ARG, "n_slots must be > 0");
+    kda::SpecLaunch p{n_seqs, n_tokens, n_heads, d_k, dtype, q, k, v, alpha, beta, const_cast<float*>(pool),
+                      n_slots, state_slot, o, u, nullptr, scale, nullptr};
+    st = status_ptr(&p.status);
+    if (st != KDA_OK) return st;
+    cudaError_t e = kda::launch_verify(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "verify launch");
+    return KDA_OK;
+}
+
+kda_status_t kda_decode_commit(int32_t n_seqs, int32_t n_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
+                               int32_t dtype, const void* k, const float* alpha, const float* u,
+                               const int32_t* n_accept, float* pool, int64_t n_slots,
+                               const int32_t* state_slot, void* stream) {
+    kda_status_t st = check_spec(n_seqs, n_tokens, n_heads, d_k, d_v, dtype, n_slots);
+    if (st != KDA_OK) return st;
+    if (n_seqs == 0) return KDA_OK;
+    KDA_REQUIRE_PTR(k, "k");
+    KDA_REQUIRE_PTR(alpha, "alpha");
+    KDA_REQUIRE_PTR(u, "u");
+    KDA_REQUIRE_PTR(n_accept, "n_accept");
+    KDA_REQUIRE_PTR(pool, "pool");
+    KDA_REQUIRE_PTR(state_slot, "state_slot");
+    if (n_slots == 0) return fail(KDA_ERR_INVALID_ARG, "n_slots must be > 0");
+    kda::SpecLaunch p{n_seqs, n_tokens, n_heads, d_k, dtype, nullptr, k, nullptr, alpha, nullptr, pool,
+                      n_slots, state_slot, nullptr, const_cast<float*>(u), n_accept, 1.f, nullptr};
+    st = status_ptr(&p.status);
+    if (st != KDA_OK) return st;
+    cudaError_t e = kda::launch_commit(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+    return KDA_OK;
+}
+
 static kda_status_t check_copy(const void* a, const void* b, int64_t n_slots, const int32_t* slots,
                                int32_t n, int32_t H, int32_t d_k, int32_t d_v) {
     kda_status_t st = check_dims(H, d_k, d_v, KDA_FP32);

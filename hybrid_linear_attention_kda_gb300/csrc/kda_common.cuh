@@ -61,6 +61,23 @@ struct DecodeLaunch {
 };
 cudaError_t launch_decode(const DecodeLaunch& p, cudaStream_t s);
 
+// Speculative decoding: T candidate tokens per sequence, [n_seqs, T, H, .] layouts.
+struct SpecLaunch {
+    int32_t n_seqs, T, H, D, dtype;
+    const void *q, *k, *v;
+    const float *alpha, *beta;
+    float* pool;
+    int64_t n_slots;
+    const int32_t* slot;
+    void* o;
+    float* u;
+    const int32_t* n_accept;
+    float scale;
+    uint32_t* status;
+};
+cudaError_t launch_verify(const SpecLaunch& p, cudaStream_t s);
+cudaError_t launch_commit(const SpecLaunch& p, cudaStream_t s);
+
 cudaError_t launch_gather(const float* pool, int64_t n_slots, const int32_t* slots, int32_t n,
                           int64_t slot_elems, float* dst, uint32_t* status, cudaStream_t s);
 cudaError_t launch_restore(const float* src, float* pool, int64_t n_slots, const int32_t* slots,

@@ -1,0 +1,251 @@
+// Speculative decoding for KDA ("Kimi K3 Tech Intro", section 6): a draft model
+// proposes several tokens per sequence and the target model checks them all in
+// one step, keeps the accepted prefix and falls back on the rest.  A recurrent
+// state cannot be rolled back, so the step is split in two:
+//
+//   verify  reads each state once and runs the T candidate tokens through it in
+//           registers, writing for every token t its output
+//               o_t = scale S_t^T q_t
+//           and its update vector
+//               u_t = beta_t (v_t - (Diag(alpha_t) S_{t-1})^T k_t),
+//           but never the state;
+//   commit  reads each state once more, applies the updates of the accepted
+//           tokens only,
+//               S <- Diag(alpha_t) S + k_t u_t^T      for t < n_accept,
+//           and writes it back (no reduction is needed: u_t is known).
+//
+// Both use the tile layout of the single-token decode kernel (one CTA per
+// (sequence, head), the whole state in registers, 16-byte coalesced access) and
+// its arithmetic in the same order, so verify(1) followed by commit(1) gives the
+// decode step's results bit for bit.  All candidate tokens' inputs are staged in
+// shared memory next to the state load, so the token loop waits on no global
+// load.
+#include "kda_common.cuh"
+
+namespace kda {
+namespace {
+
+template <int D, int NT>
+struct Tile {
+    static constexpr int TJ = D;              // columns per CTA: the whole head
+    static constexpr int LPR = TJ / 4;        // lanes per state row (one float4 each)
+    static constexpr int RPW = 32 / LPR;      // rows covered by one warp instruction
+    static constexpr int NW = NT / 32;
+    static constexpr int RPT = D / (NW * RPW);   // rows held by each thread
+    static_assert(LPR * RPW == 32 && RPT * NW * RPW == D, "tile shape");
+};
+
+// Shared memory of one verify CTA: every candidate token's alpha, k, q and v
+// ([T][D] fp32 each), its beta and q.k, staged once next to the state load.
+template <int D>
+__host__ __device__ constexpr size_t verify_smem(int T) {
+    return (size_t)T * (4 * D + 2) * sizeof(float);
+}
+
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(NT) verify_kernel(SpecLaunch p) {
+    using L = Tile<D, NT>;
+    constexpr int TJ = L::TJ, LPR = L::LPR, RPW = L::RPW, NW = L::NW, RPT = L::RPT;
+    extern __shared__ float dyn[];
+    const int nT = p.T;
+    float* s_a = dyn;                  // [T][D]
+    float* s_k = s_a + nT * D;
+    float* s_q = s_k + nT * D;
+    float* s_v = s_q + nT * D;
+    float* s_beta = s_v + nT * D;      // [T]
+    float* s_qk = s_beta + nT;         // [T]
+    __shared__ float s_red_a[NW][TJ], s_red_b[NW][TJ];
+    __shared__ __align__(16) float s_u[TJ];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t sh = blockIdx.x;           // seq * H + head
+    const int seq = (int)(sh / p.H);
+    const int h = (int)(sh - (int64_t)seq * p.H);
+    const int32_t slot = p.slot[seq];
+    if (slot < 0 || (int64_t)slot >= p.n_slots) {
+        if (tid == 0) flag(p.status, KDA_DEV_BAD_SLOT);
+        return;
+    }
+    const float* S = p.pool + ((int64_t)slot * p.H + h) * D * D;
+    const int cq = lane % LPR;
+    const int rbase = warp * (RPT * RPW) + lane / LPR;
+    float4 st[RPT];
+#pragma unroll
+    for (int m = 0; m < RPT; ++m)
+        st[m] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rbase + m * RPW) * D + 4 * cq));
+
+    // every candidate token's inputs, [n_seqs, T, H, D] rows
+    for (int e = tid; e < nT * D; e += NT) {
+        const int t = e / D, i = e - t * D;
+        const int64_t vec = (((int64_t)seq * nT + t) * p.H + h) * D;
+        s_a[e] = p.alpha[vec + i];
+        s_k[e] = Elem<T>::load(static_cast<const T*>(p.k) + vec + i);
+        s_q[e] = Elem<T>::load(static_cast<const T*>(p.q) + vec + i);
+        s_v[e] = Elem<T>::load(static_cast<const T*>(p.v) + vec + i);
+    }
+    for (int t = tid; t < nT; t += NT) s_beta[t] = p.beta[((int64_t)seq * nT + t) * p.H + h];
+    __syncthreads();
+    for (int t = warp; t < nT; t += NW) {   // q . k of every token, one warp each
+        float acc = 0.f;
+        for (int i = lane; i < D; i += 32) acc = fmaf(s_q[t * D + i], s_k[t * D + i], acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) s_qk[t] = acc;
+    }
+
+    for (int t = 0; t < nT; ++t) {
+        const float* a_t = s_a + t * D;
+        const float* k_t = s_k + t * D;
+        const float* q_t = s_q + t * D;
+        float pa[4] = {0.f, 0.f, 0.f, 0.f}, pb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) {
+            const int i = rbase + m * RPW;
+            const float ai = a_t[i];
+            const float ka = ai * k_t[i], qa = ai * q_t[i];
+            pa[0] = fmaf(ka, st[m].x, pa[0]);
+            pa[1] = fmaf(ka, st[m].y, pa[1]);
+            pa[2] = fmaf(ka, st[m].z, pa[2]);
+            pa[3] = fmaf(ka, st[m].w, pa[3]);
+            pb[0] = fmaf(qa, st[m].x, pb[0]);
+            pb[1] = fmaf(qa, st[m].y, pb[1]);
+            pb[2] = fmaf(qa, st[m].z, pb[2]);
+            pb[3] = fmaf(qa, st[m].w, pb[3]);
+        }
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                pa[c] += __shfl_xor_sync(0xffffffffu, pa[c], off);
+                pb[c] += __shfl_xor_sync(0xffffffffu, pb[c], off);
+            }
+        }
+        if (lane < LPR) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                s_red_a[warp][4 * cq + c] = pa[c];
+                s_red_b[warp][4 * cq + c] = pb[c];
+            }
+        }
+        __syncthreads();     // partial sums (and, at t = 0, every q . k) are in
+        if (tid < TJ) {
+            float a = 0.f, b = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                a += s_red_a[w][tid];
+                b += s_red_b[w][tid];
+            }
+            const int64_t vec = (((int64_t)seq * nT + t) * p.H + h) * D;
+            const float u = s_beta[t] * (s_v[t * D + tid] - a);
+            s_u[tid] = u;
+            p.u[vec + tid] = u;
+            Elem<T>::store(static_cast<T*>(p.o) + vec + tid, p.scale * fmaf(u, s_qk[t], b));
+        }
+        __syncthreads();     // u is in; the next token's partial sums may overwrite s_red
+        const float4 u4 = *reinterpret_cast<const float4*>(&s_u[4 * cq]);
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) {
+            const int i = rbase + m * RPW;
+            const float ai = a_t[i], ki = k_t[i];
+            st[m].x = fmaf(ai, st[m].x, ki * u4.x);
+            st[m].y = fmaf(ai, st[m].y, ki * u4.y);
+            st[m].z = fmaf(ai, st[m].z, ki * u4.z);
+            st[m].w = fmaf(ai, st[m].w, ki * u4.w);
+        }
+    }
+}
+
+// Shared memory of one commit CTA: alpha and k ([T][D]) and u ([T][D]) of the
+// accepted tokens.
+template <int D>
+__host__ __device__ constexpr size_t commit_smem(int T) {
+    return (size_t)T * 3 * D * sizeof(float);
+}
+
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(NT) commit_kernel(SpecLaunch p) {
+    using L = Tile<D, NT>;
+    constexpr int LPR = L::LPR, RPW = L::RPW, RPT = L::RPT;
+    extern __shared__ float dyn[];
+    const int nT = p.T;
+    float* s_a = dyn;
+    float* s_k = s_a + nT * D;
+    float* s_u = s_k + nT * D;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t sh = blockIdx.x;
+    const int seq = (int)(sh / p.H);
+    const int h = (int)(sh - (int64_t)seq * p.H);
+    const int32_t slot = p.slot[seq];
+    if (slot < 0 || (int64_t)slot >= p.n_slots) {
+        if (tid == 0) flag(p.status, KDA_DEV_BAD_SLOT);
+        return;
+    }
+    const int32_t m_acc = p.n_accept[seq];
+    if (m_acc < 0 || m_acc > nT) {
+        if (tid == 0) flag(p.status, KDA_DEV_BAD_ACCEPT);
+        return;
+    }
+    if (m_acc == 0) return;                  // nothing accepted: the state stays as it is
+    float* S = p.pool + ((int64_t)slot * p.H + h) * D * D;
+    const int cq = lane % LPR;
+    const int rbase = warp * (RPT * RPW) + lane / LPR;
+    float4 st[RPT];
+#pragma unroll
+    for (int m = 0; m < RPT; ++m)
+        st[m] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rbase + m * RPW) * D + 4 * cq));
+    for (int e = tid; e < m_acc * D; e += NT) {
+        const int t = e / D, i = e - t * D;
+        const int64_t vec = (((int64_t)seq * nT + t) * p.H + h) * D;
+        s_a[e] = p.alpha[vec + i];
+        s_k[e] = Elem<T>::load(static_cast<const T*>(p.k) + vec + i);
+        s_u[e] = p.u[vec + i];
+    }
+    __syncthreads();
+    for (int t = 0; t < m_acc; ++t) {
+        const float4 u4 = *reinterpret_cast<const float4*>(&s_u[t * D + 4 * cq]);
+#pragma unroll
+        for (int m = 0; m < RPT; ++m) {
+            const int i = rbase + m * RPW;
+            const float ai = s_a[t * D + i], ki = s_k[t * D + i];
+            st[m].x = fmaf(ai, st[m].x, ki * u4.x);
+            st[m].y = fmaf(ai, st[m].y, ki * u4.y);
+            st[m].z = fmaf(ai, st[m].z, ki * u4.z);
+            st[m].w = fmaf(ai, st[m].w, ki * u4.w);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < RPT; ++m)
+        __stcs(reinterpret_cast<float4*>(S + (int64_t)(rbase + m * RPW) * D + 4 * cq), st[m]);
+}
+
+template <typename T, int D, int NT>
+struct VerifyK {
+    static cudaError_t run(const SpecLaunch& p, cudaStream_t s) {
+        note_launch();
+        verify_kernel<T, D, NT><<<(unsigned)((int64_t)p.n_seqs * p.H), NT, verify_smem<D>(p.T), s>>>(p);
+        return cudaGetLastError();
+    }
+};
+template <typename T, int D, int NT>
+struct CommitK {
+    static cudaError_t run(const SpecLaunch& p, cudaStream_t s) {
+        note_launch();
+        commit_kernel<T, D, NT><<<(unsigned)((int64_t)p.n_seqs * p.H), NT, commit_smem<D>(p.T), s>>>(p);
+        return cudaGetLastError();
+    }
+};
+
+template <template <typename, int, int> class K>
+cudaError_t dispatch(const SpecLaunch& p, cudaStream_t s) {
+    if (p.D == 128)
+        return p.dtype == KDA_BF16 ? K<__nv_bfloat16, 128, 256>::run(p, s) : K<float, 128, 256>::run(p, s);
+    return p.dtype == KDA_BF16 ? K<__nv_bfloat16, 64, 128>::run(p, s) : K<float, 64, 128>::run(p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const SpecLaunch& p, cudaStream_t s) { return dispatch<VerifyK>(p, s); }
+cudaError_t launch_commit(const SpecLaunch& p, cudaStream_t s) { return dispatch<CommitK>(p, s); }
+
+}  // namespace kda

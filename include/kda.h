@@ -87,6 +87,7 @@ typedef enum {
 #define KDA_DEV_BAD_SEQLENS   0x4u /* cu_seqlens decreasing, or past total_tokens */
 #define KDA_DEV_BAD_ORDINAL   0x8u /* snapshot ordinal >= snap_table_stride */
 #define KDA_DEV_WAIT_TIMEOUT  0x10u /* a kernel gave up waiting on its own copies / MMAs (about 1 s) */
+#define KDA_DEV_BAD_ACCEPT    0x20u /* kda_decode_commit: an accepted count outside [0, n_tokens] */
 
 /*
  * Chunked prefill over a packed variable-length batch.
@@ -186,6 +187,53 @@ kda_status_t kda_decode_step(int32_t n_seqs, int32_t n_heads, int32_t d_k, int32
                              const float *alpha, const float *beta, float *pool,
                              int64_t n_slots, const int32_t *state_slot, void *o,
                              float scale, void *stream);
+
+/*
+ * Speculative decoding, step one: verify n_tokens candidate tokens per sequence
+ * ("Kimi K3 Tech Intro", section 6: a draft model proposes 7 tokens, the target
+ * model checks them in one step and keeps the accepted prefix).  For every
+ * (sequence, head) the state pool[state_slot[i]] is read, not written.  The
+ * call runs the candidate tokens t = 0 .. n_tokens-1 through a private copy and
+ * writes, for each t:
+ *   - o[i, t]: scale S_t^T q_t, where S_t is the state after token t;
+ *   - u[i, t]: beta_t (v_t - (Diag(alpha_t) S_{t-1})^T k_t), the update vector
+ *     that kda_decode_commit() applies.
+ * Token t of sequence i therefore sees the earlier candidates of i, as in n_tokens
+ * consecutive decode steps.
+ * Layouts (device, row-major): q, k, alpha [n_seqs, n_tokens, H, d_k];
+ * v, o, u [n_seqs, n_tokens, H, d_v]; beta [n_seqs, n_tokens, H];
+ * state_slot [n_seqs] int32.  o has the element type of q, k, v; u is fp32,
+ * caller-owned scratch.
+ * Errors:
+ *   - n_tokens outside [1, 16], and the unsupported shapes of kda_decode_step,
+ *     return an error status;
+ *   - a slot outside the pool sets KDA_DEV_BAD_SLOT and skips the sequence.
+ */
+kda_status_t kda_decode_verify(int32_t n_seqs, int32_t n_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
+                               int32_t dtype, const void *q, const void *k, const void *v,
+                               const float *alpha, const float *beta, const float *pool,
+                               int64_t n_slots, const int32_t *state_slot, void *o, float *u,
+                               float scale, void *stream);
+
+/*
+ * Speculative decoding, step two: commit the accepted tokens.  For sequence i,
+ * the call applies the updates of its first n_accept[i] candidate tokens to
+ * pool[state_slot[i]] in place:
+ *     S <- Diag(alpha_t) S + k_t u_t^T,   t = 0 .. n_accept[i]-1,
+ * where u comes from the kda_decode_verify() call on the same tokens.  The
+ * result is the state after the accepted tokens: the rejected ones leave no
+ * trace, and n_accept[i] == 0 leaves the state untouched.  One read and one
+ * write per state.
+ * Inputs: k, alpha [n_seqs, n_tokens, H, d_k]; u [n_seqs, n_tokens, H, d_v]
+ * fp32; n_accept [n_seqs] device int32 in [0, n_tokens].  Slots must be
+ * distinct.
+ * Errors: a count outside that range sets KDA_DEV_BAD_ACCEPT and a bad slot
+ * sets KDA_DEV_BAD_SLOT; either skips the sequence.
+ */
+kda_status_t kda_decode_commit(int32_t n_seqs, int32_t n_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
+                               int32_t dtype, const void *k, const float *alpha, const float *u,
+                               const int32_t *n_accept, float *pool, int64_t n_slots,
+                               const int32_t *state_slot, void *stream);
 
 /*
  * Copy n pool slots out to a contiguous buffer: dst[i] = pool[slots[i]]
