@@ -7,8 +7,10 @@
 #include <cstring>
 #include <mutex>
 #include <thread>
+#include <vector>
 
 #include "chunk_common.cuh"
+#include "kda_prefix_cache.h"
 
 namespace {
 
@@ -404,6 +406,54 @@ kda_status_t kda_snapshot_restore(const float* src, float* pool, int64_t n_slots
                                         status, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "restore launch");
     return KDA_OK;
+}
+
+kda_status_t kda_state_export(const kda_pcache* pc, const uint8_t* ids, int32_t n, int32_t capacity,
+                              const float* pool, int64_t n_slots, int32_t n_heads, int32_t d_k, int32_t d_v,
+                              float* dst, int32_t* slot_scratch, int64_t* pos_out, void* stream) {
+    if (!pc) return fail(KDA_ERR_INVALID_ARG, "kda_state_export: pc is NULL");
+    if (n < 0 || capacity < n) return fail(KDA_ERR_INVALID_ARG, "kda_state_export: need 0 <= n <= capacity");
+    if (n > 0 && !ids) return fail(KDA_ERR_INVALID_ARG, "kda_state_export: ids is NULL");
+    kda_status_t st = check_copy(pool, dst, n_slots, slot_scratch, capacity, n_heads, d_k, d_v);
+    if (st != KDA_OK || capacity == 0) return st;
+    std::vector<int32_t> slots((size_t)capacity, -1);      // the tail stays -1: zeroed by the gather
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t slot = -1;
+        int64_t pos = 0;
+        st = kda_pcache_lookup(pc, ids + 32 * (size_t)i, &slot, &pos);
+        if (st != KDA_OK) return st;
+        if (slot >= 0 && (int64_t)slot >= n_slots) slot = -1;  // outside this pool: treated as absent
+        slots[(size_t)i] = slot;
+        if (pos_out) pos_out[i] = slot >= 0 ? pos : 0;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(slot_scratch, slots.data(), sizeof(int32_t) * (size_t)capacity,
+                                    cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "slot list copy");
+    return kda_snapshot_gather(pool, n_slots, slot_scratch, capacity, n_heads, d_k, d_v, dst, stream);
+}
+
+kda_status_t kda_state_import(kda_pcache* pc, const uint8_t* ids, const int64_t* pos, int32_t n,
+                              const float* src, float* pool, int64_t n_slots, int32_t n_heads, int32_t d_k,
+                              int32_t d_v, int32_t* slot_scratch, int32_t* slots_out, void* stream) {
+    if (!pc) return fail(KDA_ERR_INVALID_ARG, "kda_state_import: pc is NULL");
+    if (n < 0) return fail(KDA_ERR_INVALID_ARG, "kda_state_import: n < 0");
+    if (n > 0 && (!ids || !pos)) return fail(KDA_ERR_INVALID_ARG, "kda_state_import: ids or pos is NULL");
+    kda_status_t st = check_copy(src, pool, n_slots, slot_scratch, n, n_heads, d_k, d_v);
+    if (st != KDA_OK || n == 0) return st;
+    std::vector<int32_t> slots((size_t)n, -1);
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t slot = -1, is_new = 0;
+        st = kda_pcache_import(pc, ids + 32 * (size_t)i, pos[i], &slot, &is_new);
+        if (st != KDA_OK) return st;
+        if (is_new && (int64_t)slot < n_slots) slots[(size_t)i] = slot;
+        if (slots_out) slots_out[i] = slots[(size_t)i];
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(slot_scratch, slots.data(), sizeof(int32_t) * (size_t)n,
+                                    cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "slot list copy");
+    return kda_snapshot_restore(src, pool, n_slots, slot_scratch, n, n_heads, d_k, d_v, stream);
 }
 
 kda_status_t kda_check_status(void* stream, int32_t timeout_ms, uint32_t* bits_out) {

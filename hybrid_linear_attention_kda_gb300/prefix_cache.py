@@ -51,6 +51,10 @@ def declare(lib):
     lib.kda_pcache_import.argtypes = [vp, vp, i64, P(i32), P(i32)]
     lib.kda_pcache_unit_hashes.restype = ctypes.c_int
     lib.kda_pcache_unit_hashes.argtypes = [vp, i64, i32, vp, i64]
+    lib.kda_state_export.restype = ctypes.c_int
+    lib.kda_state_export.argtypes = [vp, vp, i32, i32, vp, i64, i32, i32, i32, vp, vp, vp, vp]
+    lib.kda_state_import.restype = ctypes.c_int
+    lib.kda_state_import.argtypes = [vp, vp, vp, i32, vp, vp, i64, i32, i32, i32, vp, vp, vp]
 
 
 def _lib_and_check():
@@ -133,6 +137,34 @@ class PrefixCache:
         slot, pos = ctypes.c_int32(), ctypes.c_int64()
         self._check(self._lib.kda_pcache_lookup(self._h, buf, ctypes.byref(slot), ctypes.byref(pos)))
         return slot.value, pos.value
+
+    def export_states(self, ids, pool, dst, slot_scratch, stream=None):
+        """``kda_state_export``: the published states of `ids` (32-byte logical
+        ids) into dst[0 .. len(ids)), the rest of dst zeroed.  Returns the
+        positions (0 where an id was not found)."""
+        from . import _stream_handle
+        n, cap = len(ids), dst.shape[0]
+        buf = ctypes.create_string_buffer(b"".join(ids), max(1, 32 * n))
+        pos = np.zeros(max(1, n), dtype=np.int64)
+        H, d_k, d_v = pool.shape[1], pool.shape[2], pool.shape[3]
+        self._check(self._lib.kda_state_export(self._h, buf, n, cap, pool.data_ptr(), pool.shape[0], H, d_k, d_v,
+                                               dst.data_ptr(), slot_scratch.data_ptr(), pos.ctypes.data,
+                                               _stream_handle(stream)))
+        return pos[:n]
+
+    def import_states(self, ids, positions, src, pool, slot_scratch, stream=None):
+        """``kda_state_import``: register `ids` at `positions` and copy the new
+        ones from src into their slots.  Returns the slots taken (-1 = skipped)."""
+        from . import _stream_handle
+        n = len(ids)
+        buf = ctypes.create_string_buffer(b"".join(ids), max(1, 32 * n))
+        pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+        slots = np.full(max(1, n), -1, dtype=np.int32)
+        H, d_k, d_v = pool.shape[1], pool.shape[2], pool.shape[3]
+        self._check(self._lib.kda_state_import(self._h, buf, pos.ctypes.data if n else None, n, src.data_ptr(),
+                                               pool.data_ptr(), pool.shape[0], H, d_k, d_v,
+                                               slot_scratch.data_ptr(), slots.ctypes.data, _stream_handle(stream)))
+        return slots[:n]
 
     def import_state(self, logical_id: bytes, pos: int):
         """(slot, is_new) for a state that arrives from elsewhere."""

@@ -149,6 +149,52 @@ kda_status_t kda_pcache_import(kda_pcache* pc, const uint8_t* hash, int64_t pos,
 kda_status_t kda_pcache_unit_hashes(const int32_t* tokens, int64_t n_tokens, int32_t match_unit, uint8_t* out,
                                     int64_t out_len);
 
+/*
+ * State transfer by logical id ("Kimi K3 Tech Intro", section 2.4: workers pass
+ * logical prefix identifiers, not physical addresses; section 7: the tail of a
+ * transfer is zeroed so that no stale data leaks).  On one GPU this is a
+ * gather into a transfer buffer and a restore out of one.  The slot lists are
+ * resolved on the host and copied into the caller's device scratch, so the
+ * library still allocates nothing.
+ */
+
+/* Gather the published states named by ids[0 .. n) (32-byte chained hashes,
+ * host memory) into dst[0 .. capacity) (device, [capacity, H, d_k, d_v] fp32).
+ *  - Entry i < n gets the state of ids[i].  It is all zeros when the id is
+ *    unknown or not yet published.
+ *  - Entries n .. capacity-1 (the tail) are zeroed.
+ *  - pos_out[i] (host, may be NULL) receives the state's absolute position, or
+ *    0 when the id was not found.
+ * slot_scratch: device int32 [capacity], caller-owned, overwritten.  The states
+ * are read when the gather runs on `stream`, in stream order: do not let other
+ * streams overwrite those slots before it completes.
+ * Errors:
+ *   - KDA_ERR_INVALID_ARG: a NULL pointer, n < 0, capacity < n, or
+ *     n_slots < 0;
+ *   - the shape errors of kda_snapshot_gather;
+ *   - KDA_ERR_CUDA: the copy or the launch failed. */
+kda_status_t kda_state_export(const kda_pcache *pc, const uint8_t *ids, int32_t n, int32_t capacity,
+                              const float *pool, int64_t n_slots, int32_t n_heads, int32_t d_k, int32_t d_v,
+                              float *dst, int32_t *slot_scratch, int64_t *pos_out, void *stream);
+
+/* Register the states of ids[0 .. n) with positions pos[0 .. n) (host
+ * memory, positive multiples of match_unit) in this index, and copy the new
+ * ones from src[0 .. n) (device, [n, H, d_k, d_v] fp32) into the slots they
+ * got.  An id that is already registered, or that finds no slot, is skipped.
+ * slots_out[i] (host, may be NULL) is the slot taken, or -1.  The states
+ * become matchable at the next kda_pcache_end_step(pc, 1).  Call it once the
+ * restore has completed on `stream`.
+ * slot_scratch: device int32 [n], caller-owned, overwritten.
+ * Errors:
+ *   - KDA_ERR_INVALID_ARG: a NULL pointer, n < 0, or a bad position.  A bad
+ *     position stops the registration at that id: earlier ids stay registered,
+ *     and nothing is copied.
+ *   - the shape errors of kda_snapshot_restore;
+ *   - KDA_ERR_CUDA. */
+kda_status_t kda_state_import(kda_pcache *pc, const uint8_t *ids, const int64_t *pos, int32_t n,
+                              const float *src, float *pool, int64_t n_slots, int32_t n_heads, int32_t d_k,
+                              int32_t d_v, int32_t *slot_scratch, int32_t *slots_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -162,3 +162,22 @@ def test_long_prompt_plan_is_fast():
     dt = time.perf_counter() - t0
     assert p["n_units"] == 4096 and p["n_saved"] == 32
     assert dt < 5.0
+
+
+def test_state_transfer_argument_errors():
+    """Export/import reject bad arguments on the host, before any copy."""
+    pc = PrefixCache(4, retention_interval=256)
+    fake = 0x10000          # never dereferenced: every call below fails first
+    ids = bytes(64)
+    lib = pc._lib
+    assert lib.kda_state_export(None, ids, 2, 2, fake, 4, 2, 64, 64, fake, fake, None, None) == KDA_ERR_INVALID_ARG
+    assert lib.kda_state_export(pc._h, ids, 3, 2, fake, 4, 2, 64, 64, fake, fake, None, None) == KDA_ERR_INVALID_ARG
+    assert lib.kda_state_export(pc._h, None, 2, 2, fake, 4, 2, 64, 64, fake, fake, None, None) == KDA_ERR_INVALID_ARG
+    from hybrid_linear_attention_kda_gb300 import KDA_ERR_UNSUPPORTED
+    assert lib.kda_state_export(pc._h, ids, 2, 2, fake, 4, 2, 96, 96, fake, fake, None, None) == KDA_ERR_UNSUPPORTED
+    pos = np.array([256, 100], dtype=np.int64)          # the second position is not a multiple of 256
+    st = lib.kda_state_import(pc._h, ids, pos.ctypes.data, 2, fake, fake, 4, 2, 64, 64, fake, None, None)
+    assert st == KDA_ERR_INVALID_ARG
+    assert pc.stats()["entries"] == 1                   # the first id was registered before the error
+    pc.end_step(False)                                   # the caller discards it
+    assert pc.stats()["entries"] == 0
