@@ -26,6 +26,10 @@ Contents
                    a speculative decoding step: T candidate tokens run without
                    touching the state (outputs and update vectors), then the
                    accepted ones applied ("Kimi K3 Tech Intro", section 6).
+``fused_step``     one fused decode step with the layer's prologue (causal
+                   convolution with its state, q/k norm, gates) and epilogue
+                   (gated RMSNorm) around the update ("Kimi K3 Tech Intro",
+                   section 4.1).
 ``window_bound``   a rigorous upper bound on how much a state that is forgotten
                    at the start of a window can change the states inside it,
                    used to check long sequences on sampled windows.
@@ -36,3 +40,4 @@ from .positions import snapshot_positions, reusable_prefix  # noqa: F401
 from .bounds import window_bound, state_norm_bound  # noqa: F401
 from .prefix_cache import PrefixCacheIndex, block_hashes  # noqa: F401
 from .speculative import verify_steps, commit_steps  # noqa: F401
+from .fused_decode import fused_step  # noqa: F401
