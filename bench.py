@@ -429,6 +429,39 @@ def bench_ours(args, rank, world, dev, dist_on):
             "state_bytes_per_accepted_token": 3 * dd * dd * 4 / s_acc,
             "decode_state_bytes_per_token": 2 * dd * dd * 4}
 
+    # ---- fused decode step: convolution, q/k norm, gates, update, gated RMSNorm
+    fconv_w, fnorm_w = (t.to(dev) for t in inputs.gen_fused_params(dH, dd, dw["seed"]))
+    fcpool = inputs.gen_conv_states(dn, dH, dd, dw["seed"]).to(dev)
+    fins = [{k_: t.to(dev) for k_, t in inputs.gen_fused_step(dn, dH, dd, dw["seed"], 300 + s).items()}
+            for s in range(4)]
+    fy = torch.empty((dn, dH, dd), dtype=torch.bfloat16, device=dev)
+
+    def fused_once(i):
+        z = fins[i % 4]
+        kda.decode_fused(z["xq"], z["xk"], z["xv"], z["a"], z["b"], z["g"], fconv_w, fnorm_w, dpool, fcpool,
+                         dslots, fy, stream=stream)
+
+    for i in range(warm):
+        fused_once(i)
+    barrier(dist_on)
+    d0.record(stream)
+    for i in range(args.steps):
+        fused_once(i)
+    d1.record(stream)
+    barrier(dist_on)
+    fused_ms = max_over_ranks(d0.elapsed_time(d1), dist_on, dev) / args.steps
+    assert kda.kda_check_status(stream) == 0
+    fbytes = (2 * dn * dH * dd * dd * 4                   # recurrent state read + write
+              + 2 * dn * dH * 3 * 3 * dd * 2              # convolution state read + write
+              + dn * dH * (5 * dd * 2 + 2)                # xq, xk, xv, a, g, b (bf16)
+              + dn * dH * dd * 2                          # y (bf16)
+              + dH * (3 * 4 * dd + dd) * 4)               # convolution taps and norm weight
+    fused = {"workload": f"{dn} sequences x {dH} heads, d={dd}: causal convolution (width 4) with its state, "
+                         "q/k L2 norm, gates, update, gated RMSNorm in one kernel",
+             "value": fbytes / (fused_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": fused_ms,
+             "frac_of_hbm": fbytes / (fused_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+             "algorithmic_bytes_per_launch": fbytes}
+
     # ---- snapshot gather + restore of 128 states (64 KiB each)
     gsl = torch.arange(0, 2 * 128, 2, dtype=torch.int32, device=dev) % dn
     gbuf = torch.empty((128, dH, dd, dd), dtype=torch.float32, device=dev)
@@ -475,6 +508,7 @@ def bench_ours(args, rank, world, dev, dist_on):
                    "e2e": {"value": world * dbytes / (dec_e2e_ms / 1e3) / 1e9, "unit": "GB/s",
                            "ms_per_step": dec_e2e_ms, "h2d_bytes_per_step": d_h2d,
                            "d2h_bytes_per_step": d_d2h}},
+        "fused_decode": fused,
         "speculative_decode": spec,
         "snapshot_copy": {"value": copy_bytes / (copy_ms / 1e3) / 1e9, "unit": "GB/s",
                           "ms_per_step": copy_ms, "states": 128},

@@ -51,6 +51,19 @@ class PrefillArgs(ctypes.Structure):
     ]
 
 
+class FusedDecodeArgs(ctypes.Structure):
+    """Mirror of ``kda_fused_decode_args``."""
+    _fields_ = [
+        ("n_seqs", ctypes.c_int32), ("n_heads", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("conv_size", ctypes.c_int32), ("norm_eps", ctypes.c_float), ("reserved0", ctypes.c_int32),
+        ("n_slots", ctypes.c_int64),
+        ("xq", ctypes.c_void_p), ("xk", ctypes.c_void_p), ("xv", ctypes.c_void_p),
+        ("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("g", ctypes.c_void_p),
+        ("conv_w", ctypes.c_void_p), ("norm_w", ctypes.c_void_p), ("pool", ctypes.c_void_p),
+        ("conv_state", ctypes.c_void_p), ("state_slot", ctypes.c_void_p), ("y", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -83,6 +96,8 @@ def load():
                                                ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_char_p)]
     lib.kda_decode_step.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, vp, f32, vp]
+    lib.kda_decode_fused.restype = ctypes.c_int
+    lib.kda_decode_fused.argtypes = [ctypes.POINTER(FusedDecodeArgs), vp]
     lib.kda_decode_verify.restype = ctypes.c_int
     lib.kda_decode_verify.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, f32, vp]
     lib.kda_decode_commit.restype = ctypes.c_int
@@ -205,6 +220,21 @@ def kda_decode_step(q, k, v, alpha, beta, pool, state_slot, o, scale=1.0, stream
     _check(load().kda_decode_step(n, H, d_k, d_v, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
                                   _ptr(alpha), _ptr(beta), _ptr(pool), pool.shape[0],
                                   _ptr(state_slot), _ptr(o), float(scale), _stream_handle(stream)))
+
+
+def kda_decode_fused(args: FusedDecodeArgs, stream=None):
+    _check(load().kda_decode_fused(ctypes.byref(args), _stream_handle(stream)))
+
+
+def decode_fused(xq, xk, xv, a, b, g, conv_w, norm_w, pool, conv_state, state_slot, y, norm_eps=1e-6,
+                 stream=None):
+    """One fused decode step (``kda_decode_fused``): convolution, q/k norm,
+    gates, update and gated RMSNorm, with both states updated in place."""
+    n, H, d = xq.shape
+    args = FusedDecodeArgs(n, H, d, conv_w.shape[2], float(norm_eps), 0, pool.shape[0],
+                           _ptr(xq), _ptr(xk), _ptr(xv), _ptr(a), _ptr(b), _ptr(g), _ptr(conv_w),
+                           _ptr(norm_w), _ptr(pool), _ptr(conv_state), _ptr(state_slot), _ptr(y))
+    kda_decode_fused(args, stream)
 
 
 def kda_decode_verify(q, k, v, alpha, beta, pool, state_slot, o, u, scale=1.0, stream=None):

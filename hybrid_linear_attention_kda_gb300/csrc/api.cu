@@ -306,6 +306,39 @@ kda_status_t kda_decode_step(int32_t n_seqs, int32_t n_heads, int32_t d_k, int32
     return KDA_OK;
 }
 
+kda_status_t kda_decode_fused(const kda_fused_decode_args* args, void* stream) {
+    if (!args) return fail(KDA_ERR_INVALID_ARG, "args is NULL");
+    const kda_fused_decode_args& a = *args;
+    kda_status_t st = check_dims(a.n_heads, a.d, a.d, KDA_BF16);
+    if (st != KDA_OK) return st;
+    if (a.conv_size != 4) return fail(KDA_ERR_UNSUPPORTED, "conv_size must be 4 (got %d)", a.conv_size);
+    if (a.reserved0 != 0) return fail(KDA_ERR_INVALID_ARG, "reserved0 must be 0");
+    if (!(a.norm_eps >= 0.f)) return fail(KDA_ERR_INVALID_ARG, "norm_eps must be >= 0");
+    if (a.n_seqs < 0 || a.n_seqs > kMaxSeqs) return fail(KDA_ERR_INVALID_ARG, "n_seqs %d", a.n_seqs);
+    if (a.n_slots < 0) return fail(KDA_ERR_INVALID_ARG, "n_slots < 0");
+    if (a.n_seqs == 0) return KDA_OK;
+    if ((int64_t)a.n_seqs * a.n_heads > (int64_t)INT32_MAX) return fail(KDA_ERR_INVALID_ARG, "n_seqs * n_heads too large");
+    KDA_REQUIRE_PTR(a.xq, "xq");
+    KDA_REQUIRE_PTR(a.xk, "xk");
+    KDA_REQUIRE_PTR(a.xv, "xv");
+    KDA_REQUIRE_PTR(a.a, "a");
+    KDA_REQUIRE_PTR(a.b, "b");
+    KDA_REQUIRE_PTR(a.g, "g");
+    KDA_REQUIRE_PTR(a.conv_w, "conv_w");
+    KDA_REQUIRE_PTR(a.norm_w, "norm_w");
+    KDA_REQUIRE_PTR(a.pool, "pool");
+    KDA_REQUIRE_PTR(a.conv_state, "conv_state");
+    KDA_REQUIRE_PTR(a.state_slot, "state_slot");
+    KDA_REQUIRE_PTR(a.y, "y");
+    if (a.n_slots == 0) return fail(KDA_ERR_INVALID_ARG, "n_slots must be > 0");
+    kda::FusedDecodeLaunch L{a, nullptr};
+    st = status_ptr(&L.status);
+    if (st != KDA_OK) return st;
+    cudaError_t e = kda::launch_fused_decode(L, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fused decode launch");
+    return KDA_OK;
+}
+
 static kda_status_t check_spec(int32_t n_seqs, int32_t n_tokens, int32_t n_heads, int32_t d_k, int32_t d_v,
                                int32_t dtype, int64_t n_slots) {
     kda_status_t st = check_dims(n_heads, d_k, d_v, dtype);

@@ -76,6 +76,13 @@ struct SpecLaunch {
     uint32_t* status;
 };
 cudaError_t launch_verify(const SpecLaunch& p, cudaStream_t s);
+
+// One fused decode step (prologue, update, epilogue); arguments as in the C ABI.
+struct FusedDecodeLaunch {
+    kda_fused_decode_args a;
+    uint32_t* status;
+};
+cudaError_t launch_fused_decode(const FusedDecodeLaunch& L, cudaStream_t s);
 cudaError_t launch_commit(const SpecLaunch& p, cudaStream_t s);
 
 cudaError_t launch_gather(const float* pool, int64_t n_slots, const int32_t* slots, int32_t n,

@@ -147,6 +147,38 @@ def gen_token_table(vocab, H, d_k, d_v, seed, dtype=torch.bfloat16, decay="mild"
             "alpha": ab.to(torch.float32), "beta": bb.to(torch.float32)}
 
 
+FUSED_STREAM = 1_000_003
+
+
+def gen_fused_params(H, d, seed):
+    """Per-head parameters of the fused decode step: depthwise convolution taps
+    conv_w [H, 3, 4, d] ~ N(0, 0.5^2) (q, k, v) and the RMSNorm weight
+    norm_w [H, d] ~ 1 + N(0, 0.1^2), both fp32."""
+    g = _stream(seed, FUSED_STREAM)
+    conv_w = (0.5 * torch.randn((H, 3, 4, d), generator=g, dtype=torch.float64)).to(torch.float32)
+    norm_w = (1.0 + 0.1 * torch.randn((H, d), generator=g, dtype=torch.float64)).to(torch.float32)
+    return conv_w, norm_w
+
+
+def gen_fused_step(n, H, d, seed, step):
+    """Raw projections of one decode token per (sequence, head), bf16: xq, xk,
+    xv, g ~ N(0, 1); a ~ N(2, 1) (decay logits, alpha = exp(-softplus(a)) as in
+    the decay recipe above); b ~ N(0, 1) (beta logits, [n, H])."""
+    g = _stream(seed + 7919 * (step + 1), FUSED_STREAM)
+    out = {}
+    for key in ("xq", "xk", "xv", "g"):
+        out[key] = torch.randn((n, H, d), generator=g, dtype=torch.float64).to(torch.bfloat16)
+    out["a"] = (torch.randn((n, H, d), generator=g, dtype=torch.float64) + 2.0).to(torch.bfloat16)
+    out["b"] = torch.randn((n, H), generator=g, dtype=torch.float64).to(torch.bfloat16)
+    return out
+
+
+def gen_conv_states(n, H, d, seed):
+    """Convolution states [n, H, 3, 3, d] bf16 ~ N(0, 1) (previous raw inputs)."""
+    g = _stream(seed, FUSED_STREAM + 1)
+    return torch.randn((n, H, 3, 3, d), generator=g, dtype=torch.float64).to(torch.bfloat16)
+
+
 def embed(table, token_lists):
     """Packed inputs of several token-id lists: dict with q, k, v, alpha, beta
     ([sum of lengths, H, .]) and cu_seqlens."""

@@ -189,6 +189,49 @@ kda_status_t kda_decode_step(int32_t n_seqs, int32_t n_heads, int32_t d_k, int32
                              float scale, void *stream);
 
 /*
+ * One fused decode step of the whole KDA layer, after its input projection
+ * ("Kimi K3 Tech Intro", section 4.1).  The step fuses the causal convolution,
+ * the q/k norm, the gates, the recurrent update and the gated RMSNorm into one
+ * kernel.  The convolution state and the recurrent state are updated in place
+ * (section 2.1 names the two per-request states).
+ *
+ * Per (sequence, head), from the raw projections of one token:
+ *   y_x = silu(sum_tau conv_w[h, x, tau] * [C_x, x_x][tau])  for x in q, k, v
+ *                                                           (tap conv_size-1 is the token)
+ *   C_x <- the last conv_size-1 raw inputs (oldest first)
+ *   q = y_q / sqrt(|y_q|^2 + 1e-6),  k likewise,  v = y_v
+ *   alpha = exp(-softplus(a)),  beta = sigmoid(b)
+ *   S <- Diag(alpha) S + k (beta (v - (Diag(alpha) S)^T k))^T,   o = S^T q
+ *   y = norm_w[h] * o / sqrt(mean(o^2) + norm_eps) * sigmoid(g)
+ * The pages name these steps but not their forms; the forms above are this
+ * library's reading (width-4 depthwise convolution with SiLU, L2 q/k norm,
+ * sigmoid-gated RMSNorm).
+ *
+ * Layouts (device, row-major):
+ *   xq, xk, xv, a, g  bf16 [n_seqs, H, d];  b bf16 [n_seqs, H]
+ *   conv_w fp32 [H, 3, conv_size, d] (q, k, v);  norm_w fp32 [H, d]
+ *   pool fp32 [n_slots, H, d, d];  conv_state bf16 [n_slots, H, 3, conv_size-1, d]
+ *   state_slot int32 [n_seqs] (distinct);  y bf16 [n_seqs, H, d]
+ * Supported: d in {64, 128}, conv_size == 4, reserved0 == 0.  Anything else
+ * returns KDA_ERR_UNSUPPORTED / KDA_ERR_INVALID_ARG.  A slot outside the pool
+ * sets KDA_DEV_BAD_SLOT and skips the sequence.
+ */
+typedef struct {
+    int32_t n_seqs, n_heads, d, conv_size;
+    float norm_eps;
+    int32_t reserved0;
+    int64_t n_slots;
+    const void *xq, *xk, *xv, *a, *b, *g;
+    const float *conv_w, *norm_w;
+    float *pool;
+    void *conv_state;
+    const int32_t *state_slot;
+    void *y;
+} kda_fused_decode_args;
+
+kda_status_t kda_decode_fused(const kda_fused_decode_args *args, void *stream);
+
+/*
  * Speculative decoding, step one: verify n_tokens candidate tokens per sequence
  * ("Kimi K3 Tech Intro", section 6: a draft model proposes 7 tokens, the target
  * model checks them in one step and keeps the accepted prefix).  For every

@@ -139,3 +139,26 @@ def test_binding_raises_instead_of_falling_back(monkeypatch, tmp_path):
 def test_workspace_size_of_an_empty_batch_is_zero(lib):
     assert kda.kda_prefill_workspace_size(_args(n_seqs=0, total_tokens=0)) == 0
     assert torch.tensor(0).numel() == 1
+
+
+def test_fused_decode_args_struct_and_checks(lib):
+    # 4 int32, float + int32, int64, 12 pointers (LP64)
+    assert ctypes.sizeof(kda.FusedDecodeArgs) == 4 * 4 + 8 + 8 + 8 * 12
+    a = kda.FusedDecodeArgs()
+    a.n_seqs, a.n_heads, a.d, a.conv_size, a.n_slots = 1, 2, 96, 4, 1
+    assert lib.kda_decode_fused(ctypes.byref(a), None) == kda.KDA_ERR_UNSUPPORTED
+    a.d, a.conv_size = 128, 3
+    assert lib.kda_decode_fused(ctypes.byref(a), None) == kda.KDA_ERR_UNSUPPORTED
+    a.conv_size = 4
+    assert lib.kda_decode_fused(ctypes.byref(a), None) == kda.KDA_ERR_INVALID_ARG     # NULL pointers
+    a.reserved0 = 1
+    assert lib.kda_decode_fused(ctypes.byref(a), None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_fused(None, None) == kda.KDA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("T", [0, 17])
+def test_verify_rejects_token_counts(lib, T):
+    fake = 0x10000
+    st = lib.kda_decode_verify(1, T, 2, 128, 128, kda.KDA_BF16, fake, fake, fake, fake, fake, fake, 1, fake,
+                               fake, fake, 1.0, None)
+    assert st == kda.KDA_ERR_UNSUPPORTED
