@@ -69,12 +69,9 @@ __global__ void __launch_bounds__(NT) verify_kernel(SpecLaunch p) {
     const float* S = p.pool + ((int64_t)slot * p.H + h) * D * D;
     const int cq = lane % LPR;
     const int rbase = warp * (RPT * RPW) + lane / LPR;
-    float4 st[RPT];
-#pragma unroll
-    for (int m = 0; m < RPT; ++m)
-        st[m] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rbase + m * RPW) * D + 4 * cq));
 
-    // every candidate token's inputs, [n_seqs, T, H, D] rows
+    // every candidate token's inputs ([n_seqs, T, H, D] rows) first: they are
+    // small and return before the state
     for (int e = tid; e < nT * D; e += NT) {
         const int t = e / D, i = e - t * D;
         const int64_t vec = (((int64_t)seq * nT + t) * p.H + h) * D;
@@ -84,6 +81,10 @@ __global__ void __launch_bounds__(NT) verify_kernel(SpecLaunch p) {
         s_v[e] = Elem<T>::load(static_cast<const T*>(p.v) + vec + i);
     }
     for (int t = tid; t < nT; t += NT) s_beta[t] = p.beta[((int64_t)seq * nT + t) * p.H + h];
+    float4 st[RPT];
+#pragma unroll
+    for (int m = 0; m < RPT; ++m)
+        st[m] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rbase + m * RPW) * D + 4 * cq));
     __syncthreads();
     for (int t = warp; t < nT; t += NW) {   // q . k of every token, one warp each
         float acc = 0.f;
