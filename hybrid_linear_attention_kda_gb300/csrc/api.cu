@@ -121,8 +121,26 @@ int64_t max_chunks_for(const kda_prefill_args* a) {
     return a->total_tokens / kda::kC + a->n_seqs;
 }
 
+// Long sequences in a batch of few chains are split into segments that run in
+// parallel (a chain of 16,384 chunks would otherwise keep one SM busy while the
+// others idle): when the batch has fewer chains than half the SMs and at least
+// two segments' worth of tokens.
+bool split_for(const kda_prefill_args* a) {
+    if (!use_chunked(a) || a->total_tokens < 2 * kda::kSegTokens) return false;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 1 << 20;                      // unknown: assume splitting pays
+    return (int64_t)a->n_seqs * a->n_heads * 2 < sms;
+}
+
+// A split sequence of L tokens has at most L / kSegTokens + 2 segments.
+int64_t max_segs_for(const kda_prefill_args* a) { return kda::max_segments(a->total_tokens, a->n_seqs); }
+int64_t max_scratch_for(const kda_prefill_args* a) { return kda::max_segments(a->total_tokens, a->n_seqs); }
+
 struct WorkspaceLayout {
-    size_t chunk_base, chain_flag, chunk_info, records, total;
+    size_t chunk_base, chain_flag, chunk_info, records, seg_info, seg_count, seg_state, total;
+    bool split;
 };
 
 WorkspaceLayout layout_for(const kda_prefill_args* a) {
@@ -137,6 +155,16 @@ WorkspaceLayout layout_for(const kda_prefill_args* a) {
     off = round_up(off + sizeof(int4) * (size_t)max_chunks_for(a), 256);
     w.records = off;
     off += (size_t)max_chunks_for(a) * a->n_heads * kda::kRecBytes;
+    w.split = split_for(a);
+    if (w.split) {
+        off = round_up(off, 256);
+        w.seg_info = off;
+        off = round_up(off + sizeof(int4) * (size_t)max_segs_for(a), 256);
+        w.seg_count = off;
+        off = round_up(off + sizeof(int32_t) * ((size_t)a->n_seqs + 2), 256);
+        w.seg_state = off;
+        off += (size_t)max_scratch_for(a) * a->n_heads * 3 * kda::kD * kda::kD * sizeof(float);
+    }
     w.total = round_up(off, 256);
     return w;
 }
@@ -239,12 +267,38 @@ kda_status_t prefill_impl(const kda_prefill_args* a, void* stream, Marks* m) {
     c.records = ws + w.records;
     c.max_chunks = max_chunks_for(a);
     c.status = status;
+    c.split = w.split ? 1 : 0;
+    c.mode = kda::kCarryPlain;
+    c.seg_info = w.split ? reinterpret_cast<int4*>(ws + w.seg_info) : nullptr;
+    c.seg_count = w.split ? reinterpret_cast<int32_t*>(ws + w.seg_count) : nullptr;
+    c.seg_state = w.split ? reinterpret_cast<float*>(ws + w.seg_state) : nullptr;
+    c.max_segs = w.split ? max_segs_for(a) : 0;
     KDA_MARK("chunk_meta");
     cudaError_t e = kda::launch_chunk_meta(c, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill meta launch");
+    if (w.split) {
+        e = kda::launch_segment_meta(c, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill segment table launch");
+    }
     KDA_MARK("chunk_local");
     e = kda::launch_chunk_local(c, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill chunk-local launch");
+    if (w.split) {
+        // segment maps A (identity start, U~ = 0) and B (zero start), the scan of
+        // the segments' start states, then every segment in parallel
+        KDA_MARK("chunk_recur_map");
+        c.mode = kda::kCarryMap;
+        e = kda::launch_chunk_recur(c, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill segment-map launch");
+        KDA_MARK("chunk_recur_offset");
+        c.mode = kda::kCarryOffset;
+        e = kda::launch_chunk_recur(c, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill segment-offset launch");
+        KDA_MARK("segment_scan");
+        e = kda::launch_segment_scan(c, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill segment-scan launch");
+        c.mode = kda::kCarryFinal;
+    }
     KDA_MARK("chunk_recur");
     e = kda::launch_chunk_recur(c, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill chunk-recurrence launch");

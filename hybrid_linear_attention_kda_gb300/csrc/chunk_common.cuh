@@ -48,6 +48,28 @@ constexpr uint32_t kRecBytes = 74240;       // 72.5 KiB, a multiple of 256
 // of some head below it is recomputed token by token (chain flagged).
 constexpr float kGuardMin = 7.888609052210118e-31f;   // 2^-100
 
+// Long chains split into segments at absolute positions that are multiples of
+// kSegTokens.  The carry over a chunk is affine in the state, S' = A_c S + B_c,
+// so a segment's map (A, B) comes from running its chunks from the identity
+// with U~ = 0 (A) and from zero (B); a scan gives every segment's initial state,
+// then all segments run in parallel.
+constexpr int64_t kSegTokens = 65536;
+constexpr int64_t kSegChunks = kSegTokens / kC;
+
+// Upper bound on the segments of a batch (and on the scratch entries of split
+// ones): a sequence of L tokens has at most L / kSegTokens + 2.
+__host__ __device__ inline int64_t max_segments(int64_t total_tokens, int64_t n_seqs) {
+    return total_tokens / kSegTokens + 2 * n_seqs + 1;
+}
+
+// The carry kernel's passes.
+enum CarryMode : int32_t {
+    kCarryPlain = 0,    // every sequence as one chain (no segments)
+    kCarryMap = 1,      // segments of split sequences: identity start, U~ = 0, writes A
+    kCarryOffset = 2,   // segments of split sequences: zero start, writes B
+    kCarryFinal = 3,    // every segment: outputs, snapshots, final state
+};
+
 struct ChunkLaunch {
     kda_prefill_args a;
     int32_t* chunk_base;   // [n_seqs + 1]: first chunk of each sequence, total at [n_seqs]
@@ -56,6 +78,13 @@ struct ChunkLaunch {
     uint8_t* records;      // [max_chunks * H * kRecBytes]
     int64_t max_chunks;
     uint32_t* status;
+    // segments (used when split is set)
+    int32_t split;         // nonzero: sequences of >= 2 kSegTokens tokens are split
+    int32_t mode;          // CarryMode of this carry launch
+    int4* seg_info;        // [max_segs]: {sequence, first chunk within it, chunks, scratch index or -1}
+    int32_t* seg_count;    // [1 + n_seqs + 1]: segments, then each sequence's first segment (and total)
+    float* seg_state;      // [scratch, H, 3, kD, kD]: A, B, initial state of each split segment
+    int64_t max_segs;
 };
 
 // Sequence checks shared by the prefill kernels; true when the sequence is usable.
@@ -88,5 +117,7 @@ __device__ __forceinline__ bool seq_valid(const kda_prefill_args& a, int seq, in
 cudaError_t launch_chunk_meta(const ChunkLaunch& p, cudaStream_t s);
 cudaError_t launch_chunk_local(const ChunkLaunch& p, cudaStream_t s);
 cudaError_t launch_chunk_recur(const ChunkLaunch& p, cudaStream_t s);
+cudaError_t launch_segment_meta(const ChunkLaunch& p, cudaStream_t s);
+cudaError_t launch_segment_scan(const ChunkLaunch& p, cudaStream_t s);
 
 }  // namespace kda

@@ -55,6 +55,7 @@ static_assert(sizeof(Misc) <= 128, "barrier block");
 
 __device__ __forceinline__ void sts16(uint32_t saddr, uint4 v) { st_shared_v4(saddr, v.x, v.y, v.z, v.w); }
 
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -64,16 +65,39 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     const kda_prefill_args& a = p.a;
     const int H = a.n_heads;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int seq = (int)(blockIdx.x / H);
+    constexpr int mode = MODE;
     const int h = (int)(blockIdx.x % H);
+    int seq;
+    int64_t coff = 0, ncs = -1;     // this chain's first chunk within its sequence, its chunks
+    int32_t scr = -1;               // scratch index of a split segment
+    if (mode == kCarryPlain) {
+        seq = (int)(blockIdx.x / H);
+    } else {
+        const int64_t sidx = blockIdx.x / H;
+        if (sidx >= p.seg_count[0]) return;
+        const int4 si = p.seg_info[sidx];
+        seq = si.x;
+        coff = si.y;
+        ncs = si.z;
+        scr = si.w;
+        if (mode != kCarryFinal && scr < 0) return;   // only split sequences have segment maps
+    }
     int64_t tb, te, pos0;
     int32_t init;
     uint32_t bad;
     if (!seq_valid(a, seq, &tb, &te, &pos0, &init, &bad)) return;     // flagged by the meta kernel
     if (p.chain_flag[(int64_t)seq * H + h]) return;                    // recomputed token by token
-    const int64_t g0 = p.chunk_base[seq];
-    const int64_t nc = p.chunk_base[seq + 1] - g0;
-    if (nc < 0 || g0 + nc > p.max_chunks) return;
+    const int64_t g_seq = p.chunk_base[seq];
+    const int64_t nc_seq = p.chunk_base[seq + 1] - g_seq;
+    if (nc_seq < 0 || g_seq + nc_seq > p.max_chunks) return;
+    if (ncs < 0) ncs = nc_seq;
+    if (coff < 0 || coff + ncs > nc_seq) return;
+    const bool last_seg = coff + ncs == nc_seq;
+    const bool writes_out = mode == kCarryPlain || mode == kCarryFinal;
+    const int64_t g0 = g_seq + coff;
+    const int64_t nc = ncs;
+    tb += coff * kC;                // first packed token and absolute position of this chain
+    pos0 += coff * kC;
     const int64_t slot_stride = (int64_t)H * kD * kD;
     const int64_t head_off = (int64_t)h * kD * kD;
 
@@ -112,7 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     // pool slot of the snapshot after chunk lc, or -1 (none, skipped, or a bad
     // index, which `report` flags)
     auto snap_slot = [&](int64_t lc, bool report) -> int32_t {
-        if (!a.snap_table) return -1;
+        if (!a.snap_table || !writes_out) return -1;
+        // the state at a split segment's end is the next segment's scanned start:
+        // the scan writes that snapshot
+        if (scr >= 0 && !last_seg && lc == nc - 1) return -1;
         const int64_t t0 = tb + lc * kC;
         const int n = (int)(te - t0 < kC ? te - t0 : kC);
         const int64_t p_end = pos0 + lc * kC + n;
@@ -223,13 +250,15 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         const int tq = 32 * ch;                // and its 32 tokens in the U epilogue
         const uint32_t lanebase = (uint32_t)(32 * jq) << 16;
         float S[64];
-        if (init >= 0) {
-            const float* S0 = a.pool + (int64_t)init * slot_stride + head_off;
+        const float* S0 = nullptr;
+        if (mode == kCarryFinal && scr >= 0) S0 = p.seg_state + ((int64_t)scr * H * 3 + (int64_t)h * 3 + 2) * kD * kD;
+        else if ((mode == kCarryPlain || mode == kCarryFinal) && init >= 0) S0 = a.pool + (int64_t)init * slot_stride + head_off;
+        if (S0) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) S[i] = S0[(int64_t)(cbase + i) * kD + j];
         } else {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) S[i] = 0.f;
+            for (int i = 0; i < 64; ++i) S[i] = (mode == kCarryMap && cbase + i == j) ? 1.f : 0.f;
         }
         auto write_sa = [&]() {
 #pragma unroll
@@ -258,7 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
 #pragma unroll
                 for (int e8 = 0; e8 < 2; ++e8) {
                     const int cc = 4 * ch + 2 * hf + e8;
-                    const uint4 ut = *reinterpret_cast<const uint4*>(stage_p + kRecU + row64_chunk_off(j, cc));
+                    // the segment map runs with U~ = 0
+                    const uint4 ut = mode == kCarryMap ? make_uint4(0u, 0u, 0u, 0u)
+                                                       : *reinterpret_cast<const uint4*>(stage_p + kRecU + row64_chunk_off(j, cc));
                     const uint32_t uw[4] = {ut.x, ut.y, ut.z, ut.w};
                     uint32_t outw[4];
 #pragma unroll
@@ -307,8 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
                 n_snap += 1;
             }
         }
-        if (ok && a.final_state) {
-            float* dst = a.final_state + (int64_t)seq * slot_stride + head_off;
+        float* dst = nullptr;
+        if (mode == kCarryMap || mode == kCarryOffset)
+            dst = p.seg_state + ((int64_t)scr * H * 3 + (int64_t)h * 3 + (mode == kCarryMap ? 0 : 1)) * kD * kD;
+        else if (last_seg && a.final_state)
+            dst = a.final_state + (int64_t)seq * slot_stride + head_off;
+        if (ok && dst) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
         }
@@ -336,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
             for (int q4 = 0; q4 < 4; ++q4) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    if (16 * q4 + e < n)
+                    if (writes_out && 16 * q4 + e < n)
                         orow[(16 * q4 + e) * ostride] = __float2bfloat16_rn(a.scale * __uint_as_float(v[q4][e]));
             }
             // a snapshot after this chunk: from the TMEM staging to the pool's [c][j] layout
@@ -366,17 +401,161 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
+// ---------------------------------------------------------------- segments
+// The segment table: a sequence of >= 2 kSegTokens tokens is split at the
+// absolute positions that are multiples of kSegTokens (so a run resumed at such
+// a position splits the same way); every other sequence is one segment.  A few
+// sequences at most take this path (fewer chains than half the SMs), so one
+// thread builds the table.
+__global__ void segment_meta_kernel(ChunkLaunch p) {
+    if (threadIdx.x != 0) return;
+    const kda_prefill_args& a = p.a;
+    const int64_t max_scr = max_segments(a.total_tokens, a.n_seqs);
+    int64_t nseg = 0, nscr = 0;
+    for (int s = 0; s < a.n_seqs; ++s) {
+        p.seg_count[1 + s] = (int32_t)nseg;
+        int64_t tb, te, pos0;
+        int32_t init;
+        uint32_t bad;
+        if (!seq_valid(a, s, &tb, &te, &pos0, &init, &bad)) continue;
+        const int64_t nch = p.chunk_base[s + 1] - p.chunk_base[s];
+        const int64_t L = te - tb;
+        if (nch <= 0) continue;
+        if (L >= 2 * kSegTokens) {
+            for (int64_t start = pos0; start < pos0 + L && nseg < p.max_segs && nscr < max_scr;) {
+                const int64_t b = (start / kSegTokens + 1) * kSegTokens;
+                const int64_t end = b < pos0 + L ? b : pos0 + L;
+                p.seg_info[nseg++] = make_int4(s, (int32_t)((start - pos0) / kC),
+                                               (int32_t)((end - start + kC - 1) / kC), (int32_t)nscr++);
+                start = end;
+            }
+        } else if (nseg < p.max_segs) {
+            p.seg_info[nseg++] = make_int4(s, 0, (int32_t)nch, -1);
+        }
+    }
+    p.seg_count[1 + a.n_seqs] = (int32_t)nseg;
+    p.seg_count[0] = (int32_t)nseg;
+}
+
+// Initial states of the segments of one (sequence, head):
+//   S_in(0) = the sequence's initial state,  S_in(k) = A_{k-1} S_in(k-1) + B_{k-1}
+// in fp32, with the snapshot at each segment boundary taken from S_in (the
+// state the next segment continues from).
+constexpr int kScanThreads = 256;
+
+__global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(ChunkLaunch p) {
+    extern __shared__ float scan_smem[];
+    const kda_prefill_args& a = p.a;
+    const int H = a.n_heads;
+    const int seq = (int)(blockIdx.x / H), h = (int)(blockIdx.x % H);
+    const int tid = threadIdx.x;
+    const int32_t s0 = p.seg_count[1 + seq], s1 = p.seg_count[2 + seq];
+    if (s1 - s0 < 1 || p.seg_info[s0].w < 0) return;          // not split
+    if (p.chain_flag[(int64_t)seq * H + h]) return;
+    int64_t tb, te, pos0;
+    int32_t init;
+    uint32_t bad;
+    if (!seq_valid(a, seq, &tb, &te, &pos0, &init, &bad)) return;
+    constexpr int DD = kD * kD;
+    float* Scur = scan_smem;
+    float* Snew = scan_smem + DD;
+    float* Am = scan_smem + 2 * DD;
+    const int64_t head_off = (int64_t)h * DD;
+    auto seg_state = [&](int32_t scr, int which) { return p.seg_state + ((int64_t)scr * H * 3 + (int64_t)h * 3 + which) * DD; };
+    {
+        const float* S0 = init >= 0 ? a.pool + (int64_t)init * H * DD + head_off : nullptr;
+        float* dst = seg_state(p.seg_info[s0].w, 2);
+        for (int e = tid; e < DD; e += kScanThreads) {
+            const float x = S0 ? S0[e] : 0.f;
+            Scur[e] = x;
+            dst[e] = x;
+        }
+    }
+    const int j = tid & (kD - 1), rows = tid >> 7;              // column j, rows 64 * rows ..
+    for (int32_t k = s0 + 1; k < s1; ++k) {
+        const int32_t prev = p.seg_info[k - 1].w;
+        const float* A = seg_state(prev, 0);
+        const float* B = seg_state(prev, 1);
+        __syncthreads();                                         // Scur written, Am free
+        for (int e = tid; e < DD / 4; e += kScanThreads)
+            reinterpret_cast<float4*>(Am)[e] = reinterpret_cast<const float4*>(A)[e];
+        __syncthreads();
+        for (int r = 0; r < 64; ++r) {
+            const int c = 64 * rows + r;
+            const float4* arow = reinterpret_cast<const float4*>(Am + c * kD);
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 8
+            for (int c4 = 0; c4 < kD / 4; ++c4) {
+                const float4 av = arow[c4];
+                acc0 = fmaf(av.x, Scur[(4 * c4) * kD + j], acc0);
+                acc1 = fmaf(av.y, Scur[(4 * c4 + 1) * kD + j], acc1);
+                acc0 = fmaf(av.z, Scur[(4 * c4 + 2) * kD + j], acc0);
+                acc1 = fmaf(av.w, Scur[(4 * c4 + 3) * kD + j], acc1);
+            }
+            Snew[c * kD + j] = (acc0 + acc1) + B[c * kD + j];
+        }
+        __syncthreads();
+        // the segment's start state, and the snapshot at that boundary
+        const int4 si = p.seg_info[k];
+        float* dst = seg_state(si.w, 2);
+        const int64_t pstart = pos0 + (int64_t)si.y * kC;
+        float* snap = nullptr;
+        if (a.snap_table && pstart % a.snap_interval == 0) {
+            const int64_t ord = pstart / a.snap_interval - 1;
+            if (ord < a.snap_table_stride) {
+                const int32_t slot = a.snap_table[(int64_t)seq * a.snap_table_stride + ord];
+                if (slot >= 0 && (int64_t)slot < a.n_slots) snap = a.pool + (int64_t)slot * H * DD + head_off;
+            }
+        }
+        for (int e = tid; e < DD; e += kScanThreads) {
+            const float x = Snew[e];
+            dst[e] = x;
+            if (snap) snap[e] = x;
+        }
+        float* t = Scur;
+        Scur = Snew;
+        Snew = t;
+    }
+}
+
 }  // namespace
 
-cudaError_t launch_chunk_recur(const ChunkLaunch& p, cudaStream_t s) {
+cudaError_t launch_segment_meta(const ChunkLaunch& p, cudaStream_t s) {
+    note_launch();
+    segment_meta_kernel<<<1, 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_segment_scan(const ChunkLaunch& p, cudaStream_t s) {
     const int64_t blocks = (int64_t)p.a.n_seqs * p.a.n_heads;
     if (blocks == 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(chunk_recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = 3 * (size_t)kD * kD * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(segment_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    note_launch();
+    segment_scan_kernel<<<(unsigned)blocks, kScanThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_recur_mode(const ChunkLaunch& p, cudaStream_t s) {
+    const int64_t blocks = (MODE == kCarryPlain ? (int64_t)p.a.n_seqs : p.max_segs) * p.a.n_heads;
+    if (blocks == 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(chunk_recur_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     note_launch();
-    chunk_recur_kernel<<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(p);
+    chunk_recur_kernel<MODE><<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_recur(const ChunkLaunch& p, cudaStream_t s) {
+    switch (p.mode) {
+        case kCarryMap: return launch_recur_mode<kCarryMap>(p, s);
+        case kCarryOffset: return launch_recur_mode<kCarryOffset>(p, s);
+        case kCarryFinal: return launch_recur_mode<kCarryFinal>(p, s);
+        default: return launch_recur_mode<kCarryPlain>(p, s);
+    }
 }
 
 }  // namespace kda

@@ -62,11 +62,12 @@ def _oracle_tokens_per_s(data, seconds):
     return toks / secs, oracle.threads(), f"first {n_tok} tokens of each sequence ({toks} tokens, {secs:.1f} s)"
 
 
-def _prefill_case(name, data, dev, reps, oracle_seconds, dtype_name, extra=None):
+def _prefill_case(name, data, dev, reps, oracle_seconds, dtype_name, extra=None, start_pos=None):
     x = {k: data[k].to(dev) for k in ("q", "k", "v", "alpha", "beta", "cu_seqlens")}
     T, H, d = data["q"].shape
     lens = data["seq_lens"]
-    n_ord = [L // 256 for L in lens]
+    starts = [0] * len(lens) if start_pos is None else [int(p) for p in start_pos]
+    n_ord = [(s0 + L) // 256 for s0, L in zip(starts, lens)]
     table = torch.full((len(lens), max(1, max(n_ord))), -1, dtype=torch.int32)
     slot = 0
     for s, m in enumerate(n_ord):
@@ -78,9 +79,11 @@ def _prefill_case(name, data, dev, reps, oracle_seconds, dtype_name, extra=None)
     fin = torch.empty((len(lens), H, d, d), device=dev)
     ws = {}
 
+    sp = None if start_pos is None else torch.tensor(starts, dtype=torch.int32, device=dev)
+
     def call():
         out = kda.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["cu_seqlens"],
-                          total_tokens=T, pool=pool, snap_table=table, o=o, final_state=fin,
+                          total_tokens=T, start_pos=sp, pool=pool, snap_table=table, o=o, final_state=fin,
                           workspace=ws.get("w"))
         return out
 
@@ -124,9 +127,11 @@ def main(argv=None):
         data = inputs.gen_varlen_resume(w["n_seqs"], w["H"], w["d"], w["d"], w["max_len"], w["prefix_len"],
                                         w["n_resume"], w["seed"])
         data["seq_lens"] = [int(x) for x in (data["cu_seqlens"][1:] - data["cu_seqlens"][:-1])]
-        # resumed sequences start from the prefix's snapshots, zero here (same work)
+        # resumed sequences start at their positions inside the shared prefix; their
+        # initial states are zero here (the same work as resuming from a snapshot)
         rows.append(_prefill_case("varlen_64", data, dev, args.reps, args.oracle_seconds, "bf16",
-                                  {"note": "resume positions as in the workload; initial states zero"}))
+                                  {"note": "resume positions as in the workload; initial states zero"},
+                                  start_pos=data["start_pos"]))
         del data
     if "decode_512x32" in only:
         w = W["decode_512x32"]

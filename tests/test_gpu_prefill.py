@@ -376,3 +376,44 @@ def test_varlen_64_shared_prefix_resume(kda, cuda_device):
             assert rel_rms(fin[s, h].cpu(), ref["final"][s, h]) < BF16_STATE_TOL, (s, h)
         for i, (s, m) in enumerate(req):
             assert rel_rms(pool[table[s, m], h].cpu(), ref["snaps"][i, h]) < BF16_STATE_TOL
+
+
+# ------------------------------------------------------------------ long chains split into segments
+
+def test_split_chain_matches_oracle_and_resumes(kda, cuda_device):
+    """One sequence of 2^18 tokens, 4 heads, mild decay (the state carried over a
+    segment boundary matters): the chain is split at multiples of 65,536 tokens
+    and the segments run in parallel from scanned start states.  The whole run
+    is checked against the oracle; a resume at a segment boundary reproduces the
+    full run bit for bit, a resume inside a segment stays within tolerance."""
+    dev = cuda_device
+    H, d, T = 4, 128, 1 << 18
+    data = inputs.gen_prefill([T], H, d, d, 20268, decay="mild")
+    n_ord = T // 256
+    pool = torch.zeros((n_ord + n_ord, H, d, d), device=dev)
+    table = np.arange(n_ord, dtype=np.int32)[None]
+    o, fin = run_gpu(kda, dev, data, pool=pool, snap_table=table)
+    checks = [65536, 100096, 131072, 196608 + 2560]
+    ref = oracle.run(data["q"], data["k"], data["v"], data["alpha"], data["beta"], [0, T],
+                     snap_req=[(0, p // 256 - 1) for p in checks])
+    for h in range(H):
+        assert rel_rms(o[:, h].float().cpu(), ref["o"][:, h]) < BF16_OUT_TOL, h
+        assert rel_rms(fin[0, h].cpu(), ref["final"][0, h]) < BF16_STATE_TOL, h
+        for i, p in enumerate(checks):
+            assert rel_rms(pool[p // 256 - 1, h].cpu(), ref["snaps"][i, h]) < BF16_STATE_TOL, (p, h)
+
+    for p, exact in ((131072, True), (100096, False)):
+        tail = {key: data[key][p:] for key in ("q", "k", "v", "alpha", "beta")}
+        tail["cu_seqlens"] = torch.tensor([0, T - p], dtype=torch.int32)
+        table2 = np.full((1, n_ord), -1, np.int32)
+        table2[0, p // 256:] = n_ord + np.arange(n_ord - p // 256)
+        o2, fin2 = run_gpu(kda, dev, tail, start_pos=[p], init_slot=[p // 256 - 1], pool=pool,
+                           snap_table=table2)
+        if exact:
+            assert torch.equal(o2, o[p:])
+            assert torch.equal(fin2, fin)
+            assert torch.equal(pool[n_ord:2 * n_ord - p // 256], pool[p // 256:n_ord])
+        else:
+            for h in range(H):
+                assert rel_rms(o2[:, h].float().cpu(), o[p:, h].float().cpu()) < BF16_OUT_TOL
+                assert rel_rms(fin2[0, h].cpu(), fin[0, h].cpu()) < BF16_STATE_TOL
