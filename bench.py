@@ -137,10 +137,10 @@ def kernel_fingerprint():
 # DRAM bytes per launch of a prefill kernel on this workload from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (source fingerprint,
 # kernel); any other fingerprint reports null.  The capture ran 2 x 8192 tokens
-# x 32 heads (8192 items, 1,234.7 MB); chunk_local's traffic grows with the item
+# x 32 heads (8192 items, 1,228.9 MB); chunk_local's traffic grows with the item
 # count, so the 16,384-item workload here moves twice that.
 RECORDED_TRAFFIC = {
-    ("4d3f2a490fdc8494", "chunk_local"): 2 * (673_882_624 + 560_832_768),
+    ("5bd63ad06eaef6b2", "chunk_local"): 2 * (673_462_016 + 555_468_800),
 }
 
 
