@@ -417,3 +417,41 @@ def test_split_chain_matches_oracle_and_resumes(kda, cuda_device):
             for h in range(H):
                 assert rel_rms(o2[:, h].float().cpu(), o[p:, h].float().cpu()) < BF16_OUT_TOL
                 assert rel_rms(fin2[0, h].cpu(), fin[0, h].cpu()) < BF16_STATE_TOL
+
+
+def test_split_and_plain_sequences_in_one_batch(kda, cuda_device):
+    """A batch with a split chain beside plain ones: 140,000 tokens (split), a
+    3,000-token sequence resumed at position 512 from a pool state, and an empty
+    sequence; 8 heads, mild decay.  Every output, final state and snapshot
+    against the oracle."""
+    dev = cuda_device
+    H, d = 8, 128
+    lens = [140000, 3000, 0]
+    data = inputs.gen_prefill(lens, H, d, d, 20269, decay="mild")
+    starts = [0, 512, 0]
+    init_state = inputs.gen_states(1, H, d, d, 20270, std=0.05)
+    n_ord = [(s + L) // 256 for s, L in zip(starts, lens)]
+    width = max(n_ord)
+    table = np.full((3, width), -1, np.int32)
+    slot = 1                                      # slot 0 holds the resumed sequence's initial state
+    for i in range(3):
+        for m in range(starts[i] // 256, n_ord[i]):
+            table[i, m] = slot
+            slot += 1
+    pool = torch.zeros((slot, H, d, d), device=dev)
+    pool[0] = init_state[0].to(dev)
+    o, fin = run_gpu(kda, dev, data, start_pos=starts, init_slot=[-1, 0, -1], pool=pool, snap_table=table)
+    init64 = np.zeros((3, H, d, d))
+    init64[1] = init_state[0].double().numpy()
+    req = [(i, m) for i in range(3) for m in range(starts[i] // 256, n_ord[i]) if m % 37 == 0 or m == n_ord[i] - 1]
+    ref = oracle.run(data["q"], data["k"], data["v"], data["alpha"], data["beta"], data["cu_seqlens"],
+                     start_pos=starts, init_state=init64, snap_req=req)
+    cu = data["cu_seqlens"].tolist()
+    for i in range(3):
+        for h in range(H):
+            if lens[i]:
+                assert rel_rms(o[cu[i]:cu[i + 1], h].float().cpu(), ref["o"][cu[i]:cu[i + 1], h]) < BF16_OUT_TOL, (i, h)
+            assert rel_rms(fin[i, h].cpu(), ref["final"][i, h]) < BF16_STATE_TOL, (i, h)
+    for r, (i, m) in enumerate(req):
+        for h in range(H):
+            assert rel_rms(pool[table[i, m], h].cpu(), ref["snaps"][r, h]) < BF16_STATE_TOL, (i, m, h)
