@@ -76,7 +76,31 @@ __global__ void __launch_bounds__(128) probe_kernel(const __nv_bfloat16* A, cons
     if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
+// A bounded wait that runs out: an mbarrier that nothing arrives at.  The
+// wait must give up after `limit` cycles and report it; the kernel then returns.
+__global__ void wait_probe_kernel(long long limit, long long* out) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const long long t0 = clock64();
+        const bool ok = mbar_wait(&bar, 0, limit);
+        out[0] = ok ? 1 : 0;
+        out[1] = clock64() - t0;
+    }
+}
+
 }  // namespace
+
+extern "C" int wait_probe(long long limit, long long* out) {
+    wait_probe_kernel<<<1, 32>>>(limit, out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaDeviceSynchronize();
+}
 
 extern "C" int tc05_probe(const void* A, const void* B, float* D, int N, int K, int a_mn, int b_mn,
                           int* err) {

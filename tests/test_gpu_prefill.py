@@ -455,3 +455,21 @@ def test_split_and_plain_sequences_in_one_batch(kda, cuda_device):
     for r, (i, m) in enumerate(req):
         for h in range(H):
             assert rel_rms(pool[table[i, m], h].cpu(), ref["snaps"][r, h]) < BF16_STATE_TOL, (i, m, h)
+
+
+
+def test_status_check_times_out_while_the_stream_is_busy(kda, cuda_device):
+    """The host watchdog: kda_check_status with a time limit reports
+    KDA_ERR_TIMEOUT while a stream still runs (20 back-to-back prefills), leaves
+    the status word alone, and the next unlimited check drains cleanly."""
+    dev = cuda_device
+    data = inputs.gen_prefill([8192] * 4, 32, 128, 128, 20271)
+    x = to_dev(data, dev)
+    cu = data["cu_seqlens"].to(dev)
+    torch.cuda.synchronize()
+    for _ in range(20):
+        kda.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], cu)
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_check_status(timeout_ms=1)
+    assert e.value.status == kda.KDA_ERR_TIMEOUT
+    assert kda.kda_check_status() == 0

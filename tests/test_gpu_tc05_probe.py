@@ -27,6 +27,8 @@ def probe(tmp_path_factory):
     lib = ctypes.CDLL(str(out))
     lib.tc05_probe.restype = ctypes.c_int
     lib.tc05_probe.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p]
+    lib.wait_probe.restype = ctypes.c_int
+    lib.wait_probe.argtypes = [ctypes.c_longlong, ctypes.c_void_p]
     return lib
 
 
@@ -49,3 +51,16 @@ def test_tcgen05_mma_layouts(probe, cuda_device, N, K, a_mn, b_mn):
     ref = A.double() @ B.double().T
     assert torch.allclose(D.cpu().double(), ref, rtol=1e-4, atol=1e-3), \
         float((D.cpu().double() - ref).abs().max())
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable(probe, cuda_device):
+    """The kernels' mbarrier waits are bounded: a wait on a barrier that nothing
+    arrives at returns false after its limit (1e6 cycles here, about half a
+    millisecond) instead of hanging, and the GPU keeps working afterwards."""
+    out = torch.zeros(2, dtype=torch.int64, device=cuda_device)
+    assert probe.wait_probe(1_000_000, out.data_ptr()) == 0
+    ok, cycles = (int(x) for x in out.cpu())
+    assert ok == 0
+    assert 1_000_000 <= cycles < 50_000_000
+    x = torch.arange(1024, device=cuda_device, dtype=torch.float32)
+    assert float(x.sum()) == 1023 * 1024 / 2
