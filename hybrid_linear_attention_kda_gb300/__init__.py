@@ -121,12 +121,43 @@ def _check(status):
         raise KdaError(status, f"{name}: {lib.kda_last_error().decode()}")
 
 
-def _ptr(x):
-    if x is None:
-        return None
-    if isinstance(x, int):
-        return x
+def _dev(x, name, dtype=None, shape=None, device=None, min_numel=None):
+    """Address of a device tensor, after the checks the C calls cannot make.
+
+    They take bare pointers and trust the dtype, shape and dense row-major
+    layout their header states.  A mismatch would make a kernel read or write
+    outside the tensor, so it is refused here: the tensor must be on a CUDA
+    device (``device``, when given), contiguous, of ``dtype`` (one dtype or a
+    tuple) and of exactly ``shape``, or of at least ``min_numel`` elements."""
+    import torch
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor (got {type(x).__name__})")
+    if dtype is not None:
+        allowed = dtype if isinstance(dtype, tuple) else (dtype,)
+        if x.dtype not in allowed:
+            raise TypeError(f"{name} must be {' or '.join(str(t) for t in allowed)} (got {x.dtype})")
+    if shape is not None and tuple(x.shape) != tuple(int(e) for e in shape):
+        raise ValueError(f"{name} must have shape {tuple(int(e) for e in shape)} (got {tuple(x.shape)})")
+    if min_numel is not None and x.numel() < min_numel:
+        raise ValueError(f"{name} must hold at least {min_numel} elements (got {x.numel()})")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if x.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device (got {x.device})")
+    if device is not None and x.device != device:
+        raise ValueError(f"{name} is on {x.device}, the other operands on {device}")
     return x.data_ptr()
+
+
+def _opt_dev(x, name, **checks):
+    return None if x is None else _dev(x, name, **checks)
+
+
+def _dims(x, name, ndim):
+    """Shape of a tensor that must have ``ndim`` dimensions."""
+    if not hasattr(x, "shape") or len(x.shape) != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions (got {getattr(x, 'shape', None)})")
+    return tuple(int(e) for e in x.shape)
 
 
 def _stream_handle(stream):
@@ -147,6 +178,11 @@ def _dtype_code(t):
     raise TypeError(f"q/k/v must be bf16 or fp32, got {t.dtype}")
 
 
+def _torch():
+    import torch
+    return torch
+
+
 def kda_status_string(status) -> str:
     return load().kda_status_string(int(status)).decode()
 
@@ -164,28 +200,41 @@ def make_prefill_args(q, k, v, alpha, beta, cu_seqlens, total_tokens, o, *, star
                       init_slot=None, pool=None, snap_table=None, final_state=None,
                       workspace=None, scale=1.0, chunk=CHUNK, snap_interval=SNAP_INTERVAL):
     """Fill a ``PrefillArgs`` from device tensors.  ``total_tokens`` is the host
-    copy of cu_seqlens[-1]; ``snap_table`` is [n_seqs, stride] int32."""
-    T, H, d_k = q.shape
-    d_v = v.shape[2]
+    copy of cu_seqlens[-1] (at most the rows of q); ``snap_table`` is
+    [n_seqs, stride] int32.  Layouts are checked against the header's."""
+    torch = _torch()
+    T, H, d_k = _dims(q, "q", 3)
+    d_v = _dims(v, "v", 3)[2]
+    n = _dims(cu_seqlens, "cu_seqlens", 1)[0] - 1
+    if not 0 <= int(total_tokens) <= T:
+        raise ValueError(f"total_tokens {int(total_tokens)} outside [0, {T}] (the rows of q)")
+    dev = q.device
+    qk = (torch.bfloat16, torch.float32)
     a = PrefillArgs()
-    a.n_seqs = cu_seqlens.shape[0] - 1
+    a.q = _dev(q, "q", qk, (T, H, d_k))
+    a.k = _dev(k, "k", q.dtype, (T, H, d_k), dev)
+    a.v = _dev(v, "v", q.dtype, (T, H, d_v), dev)
+    a.alpha = _dev(alpha, "alpha", torch.float32, (T, H, d_k), dev)
+    a.beta = _dev(beta, "beta", torch.float32, (T, H), dev)
+    a.cu_seqlens = _dev(cu_seqlens, "cu_seqlens", torch.int32, (n + 1,), dev)
+    a.o = _dev(o, "o", v.dtype, (T, H, d_v), dev)
+    a.start_pos = _opt_dev(start_pos, "start_pos", dtype=torch.int32, shape=(n,), device=dev)
+    a.init_slot = _opt_dev(init_slot, "init_slot", dtype=torch.int32, shape=(n,), device=dev)
+    n_slots = 0 if pool is None else _dims(pool, "pool", 4)[0]
+    a.pool = _opt_dev(pool, "pool", dtype=torch.float32, shape=(n_slots, H, d_k, d_v), device=dev)
+    stride = 0 if snap_table is None else _dims(snap_table, "snap_table", 2)[1]
+    a.snap_table = _opt_dev(snap_table, "snap_table", dtype=torch.int32, shape=(n, stride), device=dev)
+    a.final_state = _opt_dev(final_state, "final_state", dtype=torch.float32, shape=(n, H, d_k, d_v), device=dev)
+    a.workspace = _opt_dev(workspace, "workspace", device=dev)
+    a.n_seqs = n
     a.n_heads, a.d_k, a.d_v = H, d_k, d_v
     a.chunk, a.snap_interval = chunk, snap_interval
     a.dtype = _dtype_code(q)
     a.scale = float(scale)
     a.total_tokens = int(total_tokens)
-    a.n_slots = 0 if pool is None else pool.shape[0]
-    a.snap_table_stride = 0 if snap_table is None else snap_table.shape[1]
+    a.n_slots = n_slots
+    a.snap_table_stride = stride
     a.reserved0 = 0
-    a.q, a.k, a.v, a.alpha, a.beta = (_ptr(x) for x in (q, k, v, alpha, beta))
-    a.cu_seqlens = _ptr(cu_seqlens)
-    a.start_pos = _ptr(start_pos)
-    a.init_slot = _ptr(init_slot)
-    a.pool = _ptr(pool)
-    a.snap_table = _ptr(snap_table)
-    a.o = _ptr(o)
-    a.final_state = _ptr(final_state)
-    a.workspace = _ptr(workspace)
     a.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return a
 
@@ -214,12 +263,21 @@ def kda_prefill_chunked_events(args: PrefillArgs, events, stream=None):
 
 
 def kda_decode_step(q, k, v, alpha, beta, pool, state_slot, o, scale=1.0, stream=None):
-    """One decode step; the states in pool[state_slot[s]] are updated in place."""
-    n, H, d_k = q.shape
-    d_v = v.shape[2]
-    _check(load().kda_decode_step(n, H, d_k, d_v, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
-                                  _ptr(alpha), _ptr(beta), _ptr(pool), pool.shape[0],
-                                  _ptr(state_slot), _ptr(o), float(scale), _stream_handle(stream)))
+    """One decode step; the states in pool[state_slot[s]] are updated in place.
+    q, k, alpha [n, H, d_k]; v, o [n, H, d_v]; beta [n, H]."""
+    torch = _torch()
+    n, H, d_k = _dims(q, "q", 3)
+    d_v = _dims(v, "v", 3)[2]
+    dev = q.device
+    ptrs = (_dev(q, "q", (torch.bfloat16, torch.float32), (n, H, d_k)),
+            _dev(k, "k", q.dtype, (n, H, d_k), dev), _dev(v, "v", q.dtype, (n, H, d_v), dev),
+            _dev(alpha, "alpha", torch.float32, (n, H, d_k), dev), _dev(beta, "beta", torch.float32, (n, H), dev))
+    n_slots = _dims(pool, "pool", 4)[0]
+    pp = _dev(pool, "pool", torch.float32, (n_slots, H, d_k, d_v), dev)
+    sp = _dev(state_slot, "state_slot", torch.int32, (n,), dev)
+    op = _dev(o, "o", q.dtype, (n, H, d_v), dev)
+    _check(load().kda_decode_step(n, H, d_k, d_v, _dtype_code(q), *ptrs, pp, n_slots, sp, op, float(scale),
+                                  _stream_handle(stream)))
 
 
 def kda_decode_fused(args: FusedDecodeArgs, stream=None):
@@ -229,45 +287,88 @@ def kda_decode_fused(args: FusedDecodeArgs, stream=None):
 def decode_fused(xq, xk, xv, a, b, g, conv_w, norm_w, pool, conv_state, state_slot, y, norm_eps=1e-6,
                  stream=None):
     """One fused decode step (``kda_decode_fused``): convolution, q/k norm,
-    gates, update and gated RMSNorm, with both states updated in place."""
-    n, H, d = xq.shape
-    args = FusedDecodeArgs(n, H, d, conv_w.shape[2], float(norm_eps), 0, pool.shape[0],
-                           _ptr(xq), _ptr(xk), _ptr(xv), _ptr(a), _ptr(b), _ptr(g), _ptr(conv_w),
-                           _ptr(norm_w), _ptr(pool), _ptr(conv_state), _ptr(state_slot), _ptr(y))
+    gates, update and gated RMSNorm, with both states updated in place.
+    xq, xk, xv, a, g, y bf16 [n, H, d]; b bf16 [n, H]; conv_w fp32 [H, 3, K, d];
+    norm_w fp32 [H, d]; pool fp32 [S, H, d, d]; conv_state bf16 [S, H, 3, K-1, d]."""
+    torch = _torch()
+    n, H, d = _dims(xq, "xq", 3)
+    K = _dims(conv_w, "conv_w", 4)[2]
+    dev = xq.device
+    bf, f32 = torch.bfloat16, torch.float32
+    vec = [_dev(t, nm, bf, (n, H, d), dev) for t, nm in ((xq, "xq"), (xk, "xk"), (xv, "xv"), (a, "a"))]
+    bp = _dev(b, "b", bf, (n, H), dev)
+    gp = _dev(g, "g", bf, (n, H, d), dev)
+    cw = _dev(conv_w, "conv_w", f32, (H, 3, K, d), dev)
+    nw = _dev(norm_w, "norm_w", f32, (H, d), dev)
+    n_slots = _dims(pool, "pool", 4)[0]
+    pp = _dev(pool, "pool", f32, (n_slots, H, d, d), dev)
+    cs = _dev(conv_state, "conv_state", bf, (n_slots, H, 3, max(K - 1, 0), d), dev)
+    sp = _dev(state_slot, "state_slot", torch.int32, (n,), dev)
+    yp = _dev(y, "y", bf, (n, H, d), dev)
+    args = FusedDecodeArgs(n, H, d, K, float(norm_eps), 0, n_slots, *vec[:3], vec[3], bp, gp, cw, nw, pp, cs, sp,
+                           yp)
     kda_decode_fused(args, stream)
 
 
 def kda_decode_verify(q, k, v, alpha, beta, pool, state_slot, o, u, scale=1.0, stream=None):
     """Run T candidate tokens per sequence without touching the states:
     q, k, alpha [n, T, H, d_k]; v, o, u [n, T, H, d_v]; beta [n, T, H]."""
-    n, T, H, d_k = q.shape
-    d_v = v.shape[3]
-    _check(load().kda_decode_verify(n, T, H, d_k, d_v, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v),
-                                    _ptr(alpha), _ptr(beta), _ptr(pool), pool.shape[0], _ptr(state_slot),
-                                    _ptr(o), _ptr(u), float(scale), _stream_handle(stream)))
+    torch = _torch()
+    n, T, H, d_k = _dims(q, "q", 4)
+    d_v = _dims(v, "v", 4)[3]
+    dev = q.device
+    ptrs = (_dev(q, "q", (torch.bfloat16, torch.float32), (n, T, H, d_k)),
+            _dev(k, "k", q.dtype, (n, T, H, d_k), dev), _dev(v, "v", q.dtype, (n, T, H, d_v), dev),
+            _dev(alpha, "alpha", torch.float32, (n, T, H, d_k), dev),
+            _dev(beta, "beta", torch.float32, (n, T, H), dev))
+    n_slots = _dims(pool, "pool", 4)[0]
+    pp = _dev(pool, "pool", torch.float32, (n_slots, H, d_k, d_v), dev)
+    sp = _dev(state_slot, "state_slot", torch.int32, (n,), dev)
+    op = _dev(o, "o", q.dtype, (n, T, H, d_v), dev)
+    up = _dev(u, "u", torch.float32, (n, T, H, d_v), dev)
+    _check(load().kda_decode_verify(n, T, H, d_k, d_v, _dtype_code(q), *ptrs, pp, n_slots, sp, op, up,
+                                    float(scale), _stream_handle(stream)))
 
 
 def kda_decode_commit(k, alpha, u, n_accept, pool, state_slot, stream=None):
-    """Apply the first n_accept[i] verified updates of sequence i to its state."""
-    n, T, H, d_k = k.shape
-    d_v = u.shape[3]
-    _check(load().kda_decode_commit(n, T, H, d_k, d_v, _dtype_code(k), _ptr(k), _ptr(alpha), _ptr(u),
-                                    _ptr(n_accept), _ptr(pool), pool.shape[0], _ptr(state_slot),
+    """Apply the first n_accept[i] verified updates of sequence i to its state:
+    k, alpha [n, T, H, d_k]; u fp32 [n, T, H, d_v] from kda_decode_verify."""
+    torch = _torch()
+    n, T, H, d_k = _dims(k, "k", 4)
+    d_v = _dims(u, "u", 4)[3]
+    dev = k.device
+    kp = _dev(k, "k", (torch.bfloat16, torch.float32), (n, T, H, d_k))
+    ap = _dev(alpha, "alpha", torch.float32, (n, T, H, d_k), dev)
+    up = _dev(u, "u", torch.float32, (n, T, H, d_v), dev)
+    np_ = _dev(n_accept, "n_accept", torch.int32, (n,), dev)
+    n_slots = _dims(pool, "pool", 4)[0]
+    pp = _dev(pool, "pool", torch.float32, (n_slots, H, d_k, d_v), dev)
+    sp = _dev(state_slot, "state_slot", torch.int32, (n,), dev)
+    _check(load().kda_decode_commit(n, T, H, d_k, d_v, _dtype_code(k), kp, ap, up, np_, pp, n_slots, sp,
                                     _stream_handle(stream)))
 
 
+def _pool_and_slots(pool, slots):
+    torch = _torch()
+    n_slots, H, d_k, d_v = _dims(pool, "pool", 4)
+    m = _dims(slots, "slots", 1)[0]
+    pp = _dev(pool, "pool", torch.float32, (n_slots, H, d_k, d_v))
+    sp = _dev(slots, "slots", torch.int32, (m,), pool.device)
+    return pp, sp, (n_slots, m, H, d_k, d_v)
+
+
 def kda_snapshot_gather(pool, slots, dst, stream=None):
-    """dst[i] = pool[slots[i]] (zeros where slots[i] == -1)."""
-    _, H, d_k, d_v = pool.shape
-    _check(load().kda_snapshot_gather(_ptr(pool), pool.shape[0], _ptr(slots), slots.shape[0],
-                                      H, d_k, d_v, _ptr(dst), _stream_handle(stream)))
+    """dst[i] = pool[slots[i]] (zeros where slots[i] == -1); dst [m, H, d_k, d_v]."""
+    pp, sp, (n_slots, m, H, d_k, d_v) = _pool_and_slots(pool, slots)
+    dp = _dev(dst, "dst", _torch().float32, (m, H, d_k, d_v), pool.device)
+    _check(load().kda_snapshot_gather(pp, n_slots, sp, m, H, d_k, d_v, dp, _stream_handle(stream)))
 
 
 def kda_snapshot_restore(src, pool, slots, stream=None):
     """pool[slots[i]] = src[i] (entries with slots[i] == -1 are skipped)."""
-    _, H, d_k, d_v = pool.shape
-    _check(load().kda_snapshot_restore(_ptr(src), _ptr(pool), pool.shape[0], _ptr(slots),
-                                       slots.shape[0], H, d_k, d_v, _stream_handle(stream)))
+    pp, sp, (n_slots, m, H, d_k, d_v) = _pool_and_slots(pool, slots)
+    srp = _dev(src, "src", _torch().float32, (m, H, d_k, d_v), pool.device)
+    _check(load().kda_snapshot_restore(srp, pp, n_slots, sp, m, H, d_k, d_v, _stream_handle(stream)))
 
 
 def kda_check_status(stream=None, timeout_ms=0):
@@ -287,9 +388,9 @@ def prefill(q, k, v, alpha, beta, cu_seqlens, total_tokens=None, *, start_pos=No
     """Allocate the outputs (and workspace) with torch, then call
     ``kda_prefill_chunked``.  Returns (o, final_state or None)."""
     import torch
-    T, H, d_k = q.shape
-    d_v = v.shape[2]
-    n = cu_seqlens.shape[0] - 1
+    T, H, d_k = _dims(q, "q", 3)
+    d_v = _dims(v, "v", 3)[2]
+    n = _dims(cu_seqlens, "cu_seqlens", 1)[0] - 1
     if total_tokens is None:
         total_tokens = T
     if o is None:
@@ -303,7 +404,7 @@ def prefill(q, k, v, alpha, beta, cu_seqlens, total_tokens=None, *, start_pos=No
     if need:
         if workspace is None or workspace.numel() * workspace.element_size() < need:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-        args.workspace = workspace.data_ptr()
+        args.workspace = _dev(workspace, "workspace", device=q.device)
         args.workspace_bytes = workspace.numel() * workspace.element_size()
     kda_prefill_chunked(args, stream)
     return o, final_state

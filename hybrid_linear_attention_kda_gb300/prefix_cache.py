@@ -142,28 +142,37 @@ class PrefixCache:
         """``kda_state_export``: the published states of `ids` (32-byte logical
         ids) into dst[0 .. len(ids)), the rest of dst zeroed.  Returns the
         positions (0 where an id was not found)."""
-        from . import _stream_handle
-        n, cap = len(ids), dst.shape[0]
+        import torch
+        from . import _dev, _dims, _stream_handle
+        n = len(ids)
+        n_slots, H, d_k, d_v = _dims(pool, "pool", 4)
+        cap = _dims(dst, "dst", 4)[0]
+        pp = _dev(pool, "pool", torch.float32, (n_slots, H, d_k, d_v))
+        dp = _dev(dst, "dst", torch.float32, (cap, H, d_k, d_v), pool.device)
+        sp = _dev(slot_scratch, "slot_scratch", torch.int32, device=pool.device, min_numel=cap)
         buf = ctypes.create_string_buffer(b"".join(ids), max(1, 32 * n))
         pos = np.zeros(max(1, n), dtype=np.int64)
-        H, d_k, d_v = pool.shape[1], pool.shape[2], pool.shape[3]
-        self._check(self._lib.kda_state_export(self._h, buf, n, cap, pool.data_ptr(), pool.shape[0], H, d_k, d_v,
-                                               dst.data_ptr(), slot_scratch.data_ptr(), pos.ctypes.data,
-                                               _stream_handle(stream)))
+        self._check(self._lib.kda_state_export(self._h, buf, n, cap, pp, n_slots, H, d_k, d_v, dp, sp,
+                                               pos.ctypes.data, _stream_handle(stream)))
         return pos[:n]
 
     def import_states(self, ids, positions, src, pool, slot_scratch, stream=None):
         """``kda_state_import``: register `ids` at `positions` and copy the new
         ones from src into their slots.  Returns the slots taken (-1 = skipped)."""
-        from . import _stream_handle
+        import torch
+        from . import _dev, _dims, _stream_handle
         n = len(ids)
+        n_slots, H, d_k, d_v = _dims(pool, "pool", 4)
+        pp = _dev(pool, "pool", torch.float32, (n_slots, H, d_k, d_v))
+        srp = _dev(src, "src", torch.float32, (n, H, d_k, d_v), pool.device)
+        sp = _dev(slot_scratch, "slot_scratch", torch.int32, device=pool.device, min_numel=n)
         buf = ctypes.create_string_buffer(b"".join(ids), max(1, 32 * n))
         pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+        if pos.shape != (n,):
+            raise ValueError(f"positions must hold one entry per id ({n}), got shape {pos.shape}")
         slots = np.full(max(1, n), -1, dtype=np.int32)
-        H, d_k, d_v = pool.shape[1], pool.shape[2], pool.shape[3]
-        self._check(self._lib.kda_state_import(self._h, buf, pos.ctypes.data if n else None, n, src.data_ptr(),
-                                               pool.data_ptr(), pool.shape[0], H, d_k, d_v,
-                                               slot_scratch.data_ptr(), slots.ctypes.data, _stream_handle(stream)))
+        self._check(self._lib.kda_state_import(self._h, buf, pos.ctypes.data if n else None, n, srp, pp, n_slots,
+                                               H, d_k, d_v, sp, slots.ctypes.data, _stream_handle(stream)))
         return slots[:n]
 
     def import_state(self, logical_id: bytes, pos: int):
