@@ -420,7 +420,9 @@ __global__ void segment_meta_kernel(ChunkLaunch p) {
         if (!seq_valid(a, s, &tb, &te, &pos0, &init, &bad)) continue;
         const int64_t nch = p.chunk_base[s + 1] - p.chunk_base[s];
         const int64_t L = te - tb;
-        if (nch <= 0) continue;
+        if (nch < 0) continue;
+        // an empty sequence is one segment of no chunks: the final pass writes
+        // its initial state (a pool slot, or zeros) as its final state
         if (L >= 2 * kSegTokens) {
             for (int64_t start = pos0; start < pos0 + L && nseg < p.max_segs && nscr < max_scr;) {
                 const int64_t b = (start / kSegTokens + 1) * kSegTokens;

@@ -28,9 +28,14 @@ def run_gpu(kda, dev, d, *, start_pos=None, init_slot=None, pool=None, snap_tabl
     sp = None if start_pos is None else torch.as_tensor(start_pos, dtype=torch.int32).to(dev)
     ins = None if init_slot is None else torch.as_tensor(init_slot, dtype=torch.int32).to(dev)
     st = None if snap_table is None else torch.as_tensor(snap_table, dtype=torch.int32).to(dev)
+    # outputs start as NaN: anything the library leaves unwritten fails the comparison
+    T, H, d_k = x["q"].shape
+    d_v = x["v"].shape[2]
+    o = torch.full((T, H, d_v), float("nan"), dtype=x["v"].dtype, device=dev)
+    fin = torch.full((cu.shape[0] - 1, H, d_k, d_v), float("nan"), device=dev)
     o, fin = kda.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], cu,
                          total_tokens=int(d["cu_seqlens"][-1]), start_pos=sp, init_slot=ins,
-                         pool=pool, snap_table=st, scale=scale)
+                         pool=pool, snap_table=st, scale=scale, o=o, final_state=fin)
     torch.cuda.synchronize()
     if check:
         assert kda.kda_check_status() == 0
@@ -421,41 +426,56 @@ def test_split_chain_matches_oracle_and_resumes(kda, cuda_device):
 
 def test_split_and_plain_sequences_in_one_batch(kda, cuda_device):
     """A batch with a split chain beside plain ones: 140,000 tokens (split), a
-    3,000-token sequence resumed at position 512 from a pool state, and an empty
-    sequence; 8 heads, mild decay.  Every output, final state and snapshot
-    against the oracle."""
+    3,000-token sequence resumed at position 512 from a pool state, an empty
+    sequence, and an empty sequence resumed at 256 from that pool state; 8
+    heads, mild decay.  Every output, final state and snapshot against the
+    oracle.  The final states start as NaN: an empty sequence's final state is
+    its initial state, written even though it has no chunk."""
     dev = cuda_device
     H, d = 8, 128
-    lens = [140000, 3000, 0]
+    lens = [140000, 3000, 0, 0]
     data = inputs.gen_prefill(lens, H, d, d, 20269, decay="mild")
-    starts = [0, 512, 0]
+    starts = [0, 512, 0, 256]
+    init_slot = [-1, 0, -1, 0]
+    n = len(lens)
     init_state = inputs.gen_states(1, H, d, d, 20270, std=0.05)
     n_ord = [(s + L) // 256 for s, L in zip(starts, lens)]
     width = max(n_ord)
-    table = np.full((3, width), -1, np.int32)
-    slot = 1                                      # slot 0 holds the resumed sequence's initial state
-    for i in range(3):
+    table = np.full((n, width), -1, np.int32)
+    slot = 1                                      # slot 0 holds the resumed sequences' initial state
+    for i in range(n):
         for m in range(starts[i] // 256, n_ord[i]):
             table[i, m] = slot
             slot += 1
     pool = torch.zeros((slot, H, d, d), device=dev)
     pool[0] = init_state[0].to(dev)
-    o, fin = run_gpu(kda, dev, data, start_pos=starts, init_slot=[-1, 0, -1], pool=pool, snap_table=table)
-    init64 = np.zeros((3, H, d, d))
-    init64[1] = init_state[0].double().numpy()
-    req = [(i, m) for i in range(3) for m in range(starts[i] // 256, n_ord[i]) if m % 37 == 0 or m == n_ord[i] - 1]
+    x = to_dev(data, dev)
+    fin = torch.full((n, H, d, d), float("nan"), device=dev)
+    o, fin = kda.prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], data["cu_seqlens"].to(dev),
+                         total_tokens=int(data["cu_seqlens"][-1]),
+                         start_pos=torch.tensor(starts, dtype=torch.int32, device=dev),
+                         init_slot=torch.tensor(init_slot, dtype=torch.int32, device=dev), pool=pool,
+                         snap_table=torch.from_numpy(table).to(dev), final_state=fin)
+    torch.cuda.synchronize()
+    assert kda.kda_check_status() == 0
+    assert torch.equal(fin[2], torch.zeros_like(fin[2]))          # empty, zero start
+    assert torch.equal(fin[3], pool[0])                           # empty, resumed: its initial state
+    init64 = np.zeros((n, H, d, d))
+    init64[1] = init64[3] = init_state[0].double().numpy()
+    req = [(i, m) for i in range(n) for m in range(starts[i] // 256, n_ord[i]) if m % 37 == 0 or m == n_ord[i] - 1]
     ref = oracle.run(data["q"], data["k"], data["v"], data["alpha"], data["beta"], data["cu_seqlens"],
                      start_pos=starts, init_state=init64, snap_req=req)
     cu = data["cu_seqlens"].tolist()
-    for i in range(3):
+    for i in range(n):
         for h in range(H):
             if lens[i]:
                 assert rel_rms(o[cu[i]:cu[i + 1], h].float().cpu(), ref["o"][cu[i]:cu[i + 1], h]) < BF16_OUT_TOL, (i, h)
-            assert rel_rms(fin[i, h].cpu(), ref["final"][i, h]) < BF16_STATE_TOL, (i, h)
+                assert rel_rms(fin[i, h].cpu(), ref["final"][i, h]) < BF16_STATE_TOL, (i, h)
+            else:
+                assert np.array_equal(fin[i, h].double().cpu().numpy(), ref["final"][i, h]), (i, h)
     for r, (i, m) in enumerate(req):
         for h in range(H):
             assert rel_rms(pool[table[i, m], h].cpu(), ref["snaps"][r, h]) < BF16_STATE_TOL, (i, m, h)
-
 
 
 def test_status_check_times_out_while_the_stream_is_busy(kda, cuda_device):
