@@ -124,23 +124,36 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- helpers
 
-def kernel_fingerprint():
-    """Hash of the CUDA sources, to tie recorded ncu traffic to the kernel it measured."""
+# The sources each prefill kernel is compiled from: its own file and the
+# headers it includes.
+KERNEL_SOURCES = {
+    "chunk_local": ("csrc/chunk_local.cu", "csrc/chunk_common.cuh", "csrc/kda_common.cuh", "csrc/tc05.cuh"),
+    "chunk_recur": ("csrc/chunk_recur.cu", "csrc/chunk_common.cuh", "csrc/kda_common.cuh", "csrc/tc05.cuh"),
+}
+
+
+def kernel_fingerprint(kernel=None):
+    """Hash of the sources a kernel is built from (of every CUDA source when
+    ``kernel`` is None), to tie recorded ncu traffic to the code it measured."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "hybrid_linear_attention_kda_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + f.read())
+    pkg = os.path.join(ROOT, "hybrid_linear_attention_kda_gb300")
+    if kernel is None:
+        files = tuple(sorted(os.path.join("csrc", fn) for fn in os.listdir(os.path.join(pkg, "csrc"))))
+    else:
+        files = KERNEL_SOURCES[kernel]
+    for rel in files + ("../include/kda.h",):
+        with open(os.path.normpath(os.path.join(pkg, rel)), "rb") as f:
+            h.update(os.path.basename(rel).encode() + f.read())
     return h.hexdigest()[:16]
 
 
 # DRAM bytes per launch of a prefill kernel on this workload from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (source fingerprint,
-# kernel); any other fingerprint reports null.  The capture ran 2 x 8192 tokens
-# x 32 heads (8192 items, 1,228.9 MB); chunk_local's traffic grows with the item
-# count, so the 16,384-item workload here moves twice that.
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (kernel, fingerprint
+# of its sources); any other fingerprint reports null.  The capture ran 2 x 8192
+# tokens x 32 heads (8192 items, 1,229.0 MB); chunk_local's traffic grows with
+# the item count, so the 16,384-item workload here moves twice that.
 RECORDED_TRAFFIC = {
-    ("5bd63ad06eaef6b2", "chunk_local"): 2 * (673_462_016 + 555_468_800),
+    ("chunk_local", "9401a4878e65e1fc"): 2 * (673_448_448 + 555_532_288),
 }
 
 
@@ -287,7 +300,7 @@ def bench_ours(args, rank, world, dev, dist_on):
         dom_bytes = path_bytes
         dom_note = "the whole path's algorithmic bytes"
     fp = kernel_fingerprint()
-    traffic = RECORDED_TRAFFIC.get((fp, dom_name))
+    traffic = RECORDED_TRAFFIC.get((dom_name, kernel_fingerprint(dom_name))) if dom_name in KERNEL_SOURCES else None
     roofline = {"bound": "hbm", "kernel": dom_name,
                 "achieved": dom_bytes / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": dom_bytes / (dom_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
