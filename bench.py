@@ -556,11 +556,7 @@ def bench_ours(args, rank, world, dev, dist_on):
         "steps": args.steps, "warmup": warm, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), alpha=exp(-softplus(N(0,1)+2)), beta=sigmoid(N(0,1)))",
-        "config": {"workload": f"{PREFILL_CFG}: {n} sequences x {T} tokens, H={H}, d_k=d_v={d}, "
-                               "bf16 q/k/v/o, fp32 alpha/beta/state, chunk 64, snapshot every 256 "
-                               "tokens into a block-indexed pool, zero initial state",
-                   "l2": f"inputs larger than L2: {path_bytes / 1e9:.2f} GB of algorithmic traffic per step",
-                   "parallelism": f"replicas x{world}"},
+        "config": prefill_config(world),
         "roofline": roofline,
         "path": path,
         "tensor": tensor,
@@ -629,11 +625,25 @@ def bench_prefix_cache(n_req=2000, seed=20266):
             "prompt_tokens_reused": reused / max(1, tokens), "host": "1 thread"}
 
 
+def prefill_config(world):
+    """The prefill workload as both arms name it in their JSON lines."""
+    from hybrid_linear_attention_kda_gb300 import inputs
+    w = inputs.WORKLOADS[PREFILL_CFG]
+    n, T, H, d = w["n_seqs"], w["T"], w["H"], w["d"]
+    path_bytes = n * T * H * PREFILL_BYTES_PER_TH + n * H * d * d * 4
+    return {"workload": f"{PREFILL_CFG}: {n} sequences x {T} tokens, H={H}, d_k=d_v={d}, "
+                        "bf16 q/k/v/o, fp32 alpha/beta/state, chunk 64, snapshot every 256 "
+                        "tokens into a block-indexed pool, zero initial state",
+            "l2": f"inputs larger than L2: {path_bytes / 1e9:.2f} GB of algorithmic traffic per step",
+            "parallelism": f"replicas x{world}"}
+
+
 # ----------------------------------------------------------------------------- reference arm
 
-def bench_reference(args):
+def bench_reference(args, world=1):
     """The float64 oracle as it stands, on the host cores: each step a bounded
-    sample of the prefill workload."""
+    sample of the prefill workload.  Under a launch of ``world`` ranks only rank
+    0 runs it; its line names the same configuration as the GPU arm's."""
     from hybrid_linear_attention_kda_gb300 import inputs
     w = inputs.WORKLOADS[PREFILL_CFG]
     host = inputs.gen_prefill([w["T"]] * w["n_seqs"], w["H"], w["d"], w["d"], w["seed"])
@@ -652,7 +662,7 @@ def bench_reference(args):
             "n_gpus": 1, "steps": args.steps, "warmup": warm,
             "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{PREFILL_CFG} (bounded sample per step)"},
+            "config": prefill_config(world),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -677,7 +687,7 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(bench_reference(args)), flush=True)
+            print(json.dumps(bench_reference(args, world)), flush=True)
         return
 
     dev = torch.device("cuda", local)
