@@ -478,6 +478,23 @@ def test_split_and_plain_sequences_in_one_batch(kda, cuda_device):
             assert rel_rms(pool[table[i, m], h].cpu(), ref["snaps"][r, h]) < BF16_STATE_TOL, (i, m, h)
 
 
+@pytest.mark.parametrize("dtype, d", [(torch.bfloat16, 128), (torch.float32, 128), (torch.bfloat16, 64)])
+def test_all_empty_batch_writes_the_initial_states(kda, cuda_device, dtype, d):
+    """Three empty sequences (total_tokens = 0) on the chunked path (bf16,
+    d = 128) and the token path: nothing to compute, but every final state is
+    written: zeros without an initial slot, the slot's state when resumed."""
+    dev = cuda_device
+    H = 4
+    data = inputs.gen_prefill([0, 0, 0], H, d, d, 20272, dtype=dtype)
+    pool = inputs.gen_states(2, H, d, d, 20273, std=0.05).to(dev)
+    before = pool.clone()
+    o, fin = run_gpu(kda, dev, data, start_pos=[0, 256, 512], init_slot=[-1, 0, 1], pool=pool)
+    assert o.shape[0] == 0
+    assert torch.equal(fin[0], torch.zeros_like(fin[0]))
+    assert torch.equal(fin[1], pool[0]) and torch.equal(fin[2], pool[1])
+    assert torch.equal(pool, before)
+
+
 def test_status_check_times_out_while_the_stream_is_busy(kda, cuda_device):
     """The host watchdog: kda_check_status with a time limit reports
     KDA_ERR_TIMEOUT while a stream still runs (20 back-to-back prefills), leaves

@@ -127,6 +127,30 @@ def test_speculative_loop_keeps_only_accepted_tokens(kda, cuda_device):
                 assert frob_rel(got_o[cu[i]:cu[i + 1], h], ref["o"][cu[i]:cu[i + 1], h]) < BF16_OUT_TOL, (i, h)
 
 
+@pytest.mark.parametrize("T", [3, 16])
+def test_verify_and_commit_at_other_candidate_counts(kda, cuda_device, T):
+    """An odd candidate count and the largest one the call takes (16)."""
+    dev = cuda_device
+    n, H, d = 4, 2, 128
+    S0 = inputs.gen_states(n, H, d, d, 71 + T, std=0.05)
+    pool = S0.to(dev).clone()
+    slots = torch.arange(n, dtype=torch.int32, device=dev)
+    z = _tokens(n, T, H, d, 72 + T, 0, torch.bfloat16)
+    zd, o, u = _verify(kda, dev, z, pool, slots)
+    accept = torch.tensor([T, 0, 1, T - 1], dtype=torch.int32)
+    kda.kda_decode_commit(zd["k"], zd["alpha"], u, accept.to(dev), pool, slots)
+    torch.cuda.synchronize()
+    assert kda.kda_check_status() == 0
+    o_ref, u_ref, _ = oracle.verify_steps(S0.double().numpy(), z["q"], z["k"], z["v"], z["alpha"], z["beta"])
+    S_ref = oracle.commit_steps(S0.double().numpy(), z["k"], z["alpha"], u_ref, accept.tolist())
+    for i in range(n):
+        for h in range(H):
+            assert frob_rel(o[i, :, h].float().cpu(), o_ref[i, :, h]) < BF16_OUT_TOL, (i, h)
+            assert frob_rel(u[i, :, h].cpu(), u_ref[i, :, h]) < FP32_TOL, (i, h)
+            assert frob_rel(pool[i, h].cpu(), S_ref[i, h]) < FP32_TOL, (i, h)
+    assert torch.equal(pool[1], S0[1].to(dev))                 # none accepted: untouched
+
+
 def test_bad_accept_and_slot_are_flagged(kda, cuda_device):
     dev = cuda_device
     n, T, H, d = 4, 4, 2, 64
