@@ -105,7 +105,8 @@ typedef enum {
  * -1 (snapshot ordinals are absolute, so a resumed sequence continues the
  * numbering of the run it resumes).  snap_table may be NULL (no snapshots).
  * The states after each sequence's last token go to final_state
- * [n_seqs, H, d_k, d_v] fp32 unless it is NULL.  Outputs go to o.
+ * [n_seqs, H, d_k, d_v] fp32 unless it is NULL; an empty sequence's final
+ * states are its initial states.  Outputs go to o.
  *
  * Chunks are aligned to absolute multiples of `chunk`, and every reduction has
  * a fixed order, so a resumed run reproduces a full run bit for bit.
