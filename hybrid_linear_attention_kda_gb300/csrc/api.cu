@@ -203,7 +203,12 @@ const char* kda_status_string(kda_status_t s) {
 const char* kda_last_error(void) { return g_last_error; }
 
 size_t kda_prefill_workspace_size(const kda_prefill_args* a) {
-    if (!a || a->n_seqs < 0 || a->n_seqs > kMaxSeqs) return 0;
+    // the size checks of validate_prefill, without recording an error
+    if (!a || a->n_seqs < 0 || a->n_seqs > kMaxSeqs || a->n_heads <= 0) return 0;
+    if (a->d_k != a->d_v || (a->d_k != 64 && a->d_k != 128)) return 0;
+    if (a->dtype != KDA_BF16 && a->dtype != KDA_FP32) return 0;
+    if (a->chunk != kda::kC || a->snap_interval != 256) return 0;
+    if (a->total_tokens < 0 || a->total_tokens > (int64_t)INT32_MAX) return 0;
     return workspace_bytes_for(a);
 }
 

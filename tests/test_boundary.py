@@ -141,6 +141,18 @@ def test_workspace_size_of_an_empty_batch_is_zero(lib):
     assert torch.tensor(0).numel() == 1
 
 
+def test_workspace_size_is_zero_for_invalid_sizes(lib):
+    """The header promises 0 when the sizes are invalid; no size wraps around."""
+    assert kda.kda_prefill_workspace_size(_args()) > 0
+    for over in (dict(n_heads=0), dict(n_heads=-3), dict(d_k=96, d_v=96), dict(d_k=128, d_v=64),
+                 dict(dtype=7), dict(chunk=32), dict(snap_interval=128), dict(total_tokens=-64),
+                 dict(total_tokens=1 << 31), dict(n_seqs=-1), dict(n_seqs=(1 << 20) + 1)):
+        assert kda.kda_prefill_workspace_size(_args(**over)) == 0, over
+    # the token path (fp32, or d = 64) needs no workspace
+    assert kda.kda_prefill_workspace_size(_args(dtype=kda.KDA_FP32)) == 0
+    assert kda.kda_prefill_workspace_size(_args(d_k=64, d_v=64)) == 0
+
+
 def test_fused_decode_args_struct_and_checks(lib):
     # 4 int32, float + int32, int64, 12 pointers (LP64)
     assert ctypes.sizeof(kda.FusedDecodeArgs) == 4 * 4 + 8 + 8 + 8 * 12
