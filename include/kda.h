@@ -164,7 +164,7 @@ kda_status_t kda_prefill_chunked_events(const kda_prefill_args *args, void *stre
  * arguments (args->workspace and args->workspace_bytes are ignored), with the
  * prefill's scratch taken from a 64 MiB array in the library's own static device
  * memory, which every GPU that loads the library holds until process exit.  The
- * paper has no counterpart to this call; it exists for serving code whose device
+ * pages describe no counterpart to this call; it exists for serving code whose device
  * memory is all reserved up front, or that may not allocate on its latency
  * path.  Allocates nothing.  Returns KDA_ERR_UNSUPPORTED when
  * kda_prefill_workspace_size(args) exceeds 64 MiB.  All calls share the array:
