@@ -84,6 +84,8 @@ class ClockSampler:
         self.sel = ["-i", bus] if bus else []
 
     def start(self):
+        """Start sampling; the caller keeps the GPU busy from here on, so that
+        every sample is taken under load."""
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
@@ -92,7 +94,6 @@ class ClockSampler:
                  "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
 
     def stop(self):
         if self.proc is None:
@@ -272,20 +273,36 @@ def bench_ours(args, rank, world, dev, dist_on):
             e.record(stream)          # create the events before the timed region
     torch.cuda.synchronize(dev)
 
-    # ---- device-resident timed region
+    def soak(seconds):
+        """The same step, untimed, back to back for about `seconds`."""
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            for _ in range(8):
+                prefill_once()
+            torch.cuda.synchronize(dev)
+
+    # ---- device-resident timed region.  nvidia-smi samples every 200 ms, far
+    # longer than the timed steps, so the sampler runs over a window in which
+    # the same step keeps the GPU busy: 0.6 s before the timed region (while the
+    # sampler starts), the region itself, and 0.4 s after it.
     clocks = ClockSampler(dev)
     clocks.start()
+    soak(0.6)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     recorded = []
+    torch.cuda.synchronize(dev)
     barrier(dist_on)
     launches0 = kda.kda_launch_count()
     ev0.record(stream)
     for i in range(args.steps):
         recorded.append(kda.kda_prefill_chunked_events(pargs, marks[i], stream))
     ev1.record(stream)
+    torch.cuda.synchronize(dev)
     barrier(dist_on)
     launches = kda.kda_launch_count() - launches0
+    soak(0.4)
     clk = clocks.stop()
+    clk["window"] = "0.6 s before to 0.4 s after the timed region, the same step running throughout"
     value, total_ms = replica_throughput(total * args.steps, ev0.elapsed_time(ev1), world, dist_on, dev)
     ms_per_step = total_ms / args.steps
     assert kda.kda_check_status(stream) == 0
