@@ -301,7 +301,10 @@ kda_status_t kda_snapshot_restore(const float *src, float *pool, int64_t n_slots
  * without limit), then read and clear the current device's status word.
  * Returns KDA_OK, KDA_ERR_DEVICE_STATUS (bits in *bits_out when non-NULL),
  * KDA_ERR_TIMEOUT (the word is left untouched) or KDA_ERR_CUDA.  Calls on
- * several streams of one device share the word.
+ * several streams of one device share the word.  Only `stream` is drained: a
+ * library kernel still running on another stream can set a bit between the
+ * read and the clear, and that bit is lost.  For an exact account, check once
+ * the device's other streams have drained as well.
  */
 kda_status_t kda_check_status(void *stream, int32_t timeout_ms, uint32_t *bits_out);
 
