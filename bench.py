@@ -227,6 +227,176 @@ def oracle_prefill_sample(data, seconds_target=10.0):
 
 # ----------------------------------------------------------------------------- our arm
 
+def make_pool_table(lens, starts, H, d, dev, extra_slots=0):
+    """A pool with one slot per snapshot the batch writes (after ``extra_slots``
+    leading slots) and the matching [n, stride] table."""
+    n_ord = [(s0 + L) // 256 for s0, L in zip(starts, lens)]
+    width = max(1, max(n_ord) if n_ord else 1)
+    table = torch.full((len(lens), width), -1, dtype=torch.int32)
+    slot = extra_slots
+    n_snap = 0
+    for i, (s0, m) in enumerate(zip(starts, n_ord)):
+        first = s0 // 256
+        if m > first:
+            table[i, first:m] = torch.arange(slot, slot + m - first, dtype=torch.int32)
+            slot += m - first
+            n_snap += m - first
+    pool = torch.zeros((max(1, slot), H, d, d), dtype=torch.float32, device=dev)
+    return pool, table.to(dev), n_snap
+
+
+def prefill_method_bytes(tokens, H, d, n_snap, n_final, n_init):
+    """The method's own HBM traffic for a prefill (no intermediate of any design):
+    per token-head q, k, v (bf16), alpha (fp32), beta, o (bf16); every fp32 state
+    written (snapshots, final states) or read (initial states)."""
+    th = tokens * H
+    state = H * d * d * 4
+    return th * (3 * d * 2 + d * 4 + 4 + d * 2) + (n_snap + n_final + n_init) * state
+
+
+def time_prefill(kda, lib, pargs, stream, dev, steps, warm, dist_on, clocks_too=True):
+    """CUDA-event time of ``steps`` plain kda_prefill_chunked calls after ``warm``
+    untimed ones, with nvidia-smi clocks sampled over the timed region (the same
+    step keeps the GPU busy from 0.6 s before to 0.4 s after it).  Returns
+    (ms per step, clock record, kernels launched in the timed region)."""
+    import ctypes
+    pref = ctypes.byref(pargs)
+    sh = stream.cuda_stream
+
+    def once():
+        st = lib.kda_prefill_chunked(pref, sh)
+        if st != 0:
+            raise RuntimeError(f"prefill failed: {kda.kda_status_string(st)}: {lib.kda_last_error()}")
+
+    for _ in range(warm):
+        once()
+    torch.cuda.synchronize(dev)
+    assert kda.kda_check_status(stream) == 0
+
+    def soak(seconds):
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            for _ in range(4):
+                once()
+            torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(dev) if clocks_too else None
+    if clocks:
+        clocks.start()
+        soak(0.6)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(dist_on)
+    launches0 = kda.kda_launch_count()
+    ev0.record(stream)
+    for _ in range(steps):
+        once()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist_on)
+    launches = kda.kda_launch_count() - launches0
+    clk = None
+    if clocks:
+        soak(0.4)
+        clk = clocks.stop()
+        clk["window"] = "0.6 s before to 0.4 s after the timed region, the same step running throughout"
+    assert kda.kda_check_status(stream) == 0
+    return ev0.elapsed_time(ev1) / steps, clk, launches
+
+
+def stage_times(kda, pargs, stream, dev, steps):
+    """Per-kernel CUDA-event times (ms per step) from a separate pass of the
+    instrumented entry point, which records an event before each kernel."""
+    n_marks = 12
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(n_marks)] for _ in range(steps)]
+    for evs in marks:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    recorded = [kda.kda_prefill_chunked_events(pargs, marks[i], stream) for i in range(steps)]
+    torch.cuda.synchronize(dev)
+    stages = {}
+    for rec in recorded:
+        for (name, e_a), (_, e_b) in zip(rec[:-1], rec[1:]):
+            stages[name] = stages.get(name, 0.0) + e_a.elapsed_time(e_b) / steps
+    assert kda.kda_check_status(stream) == 0
+    return stages
+
+
+def roofline_of(stages, method_bytes, peaks, dominant_traffic=None):
+    """The dominant kernel's roofline: the method's algorithmic bytes of one
+    step (the per-token-head figure times the token-heads one launch covers)
+    over that kernel's time, against the measured HBM copy bandwidth."""
+    dom_name, dom_ms = max(stages.items(), key=lambda kv: kv[1])
+    achieved = method_bytes / (dom_ms / 1e3) / 1e9
+    return {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": dominant_traffic,
+            "peak_source": peaks["source"] + " (MEASURED_PEAKS hbm_gbs)" if peaks["source"] == "measured"
+            else peaks["source"], "algorithmic_bytes_per_launch": method_bytes, "ms_per_launch": dom_ms,
+            "bytes_counted": "the method's bytes: q, k, v, alpha, beta, o per token-head and every fp32 "
+                             "state snapshot / final state written; no intermediate of this design"}
+
+
+def bench_extra_workload(name, kda, lib, dev, stream, peaks, steps, warm, dist_on):
+    """Tokens/s and roofline fraction of the 2^20-token sequence or the mixed
+    varlen batch, inputs drawn on the device (same recipe, float32 draws)."""
+    from hybrid_linear_attention_kda_gb300 import inputs
+    w = inputs.WORKLOADS[name]
+    H, d = w["H"], w["d"]
+    if name == "long_1m":
+        data = inputs.gen_prefill_device([w["T"]], H, d, d, w["seed"], dev)
+        starts, lens = [0], [w["T"]]
+        init_slot = None
+        pool, table, n_snap = make_pool_table(lens, starts, H, d, dev)
+        n_init = 0
+        desc = (f"long_1m: 1 sequence x {w['T']} tokens, H={H}, d_k=d_v={d}, bf16 q/k/v/o, fp32 gates/state, "
+                "snapshot every 256 tokens (4096 per head), zero initial state")
+    else:
+        data = inputs.gen_varlen_resume_device(w["n_seqs"], H, d, d, w["max_len"], w["prefix_len"],
+                                               w["n_resume"], w["seed"], dev)
+        lens_full = data["lens"]
+        starts = data["start_pos"].tolist()
+        lens = [L - s0 for L, s0 in zip(lens_full, starts)]
+        n_pref = w["prefix_len"] // 256
+        pool, table, n_snap = make_pool_table(lens, starts, H, d, dev, extra_slots=n_pref)
+        # the shared prefix's snapshots fill slots [0, n_pref) first (not timed)
+        pr = data["prefix"]
+        ptab = torch.arange(n_pref, dtype=torch.int32, device=dev)[None]
+        kda.prefill(pr["q"], pr["k"], pr["v"], pr["alpha"], pr["beta"], pr["cu_seqlens_dev"],
+                    total_tokens=w["prefix_len"], pool=pool, snap_table=ptab, want_final=False)
+        init_slot = torch.tensor([(p // 256 - 1) if p > 0 else -1 for p in starts], dtype=torch.int32,
+                                 device=dev)
+        n_init = sum(1 for p in starts if p > 0)
+        desc = (f"varlen_64: {w['n_seqs']} sequences, lengths uniform in [1, {w['max_len']}], "
+                f"{w['n_resume']} resumed from a shared {w['prefix_len']}-token prefix's snapshots, H={H}, "
+                f"d_k=d_v={d}, bf16 q/k/v/o, fp32 gates/state, snapshot every 256 tokens")
+    total = int(data["cu_seqlens"][-1])
+    n = len(lens)
+    o = torch.empty((total, H, d), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((n, H, d, d), dtype=torch.float32, device=dev)
+    sp = torch.tensor(starts, dtype=torch.int32, device=dev)
+    pargs = kda.make_prefill_args(data["q"], data["k"], data["v"], data["alpha"], data["beta"],
+                                  data["cu_seqlens_dev"], total, o, start_pos=sp, init_slot=init_slot,
+                                  pool=pool, snap_table=table, final_state=fin)
+    need = kda.kda_prefill_workspace_size(pargs)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    pargs.workspace, pargs.workspace_bytes = ws.data_ptr(), need
+    ms, clk, launches = time_prefill(kda, lib, pargs, stream, dev, steps, warm, dist_on)
+    stages = stage_times(kda, pargs, stream, dev, min(steps, 3))
+    mb = prefill_method_bytes(total, H, d, n_snap, n, n_init)
+    out = {"workload": desc, "value": total / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+           "steps": steps, "tokens_per_step": total, "gpu_launches": launches,
+           "roofline": roofline_of(stages, mb, peaks),
+           "path": {"achieved_gbs": mb / (ms / 1e3) / 1e9, "frac_of_hbm": mb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                    "algorithmic_bytes_per_step": mb},
+           "stage_ms": stages, "clocks": clk,
+           "l2": f"inputs larger than L2: {mb / 1e9:.2f} GB of algorithmic traffic per step",
+           "data": "synthetic, drawn on the device (seeded torch generator, float32 draws, same recipe)"}
+    del data, o, fin, pool, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def bench_ours(args, rank, world, dev, dist_on):
     import hybrid_linear_attention_kda_gb300 as kda
     from hybrid_linear_attention_kda_gb300 import inputs
@@ -251,90 +421,46 @@ def bench_ours(args, rank, world, dev, dist_on):
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
         pargs.workspace, pargs.workspace_bytes = ws.data_ptr(), need
     stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
     import ctypes
     pref = ctypes.byref(pargs)
 
     def prefill_once():
-        st = lib.kda_prefill_chunked(pref, sh)
+        st = lib.kda_prefill_chunked(pref, stream.cuda_stream)
         if st != 0:
             raise RuntimeError(f"prefill failed: {kda.kda_status_string(st)}: {lib.kda_last_error()}")
 
     warm = max(3, args.warmup)
-    for _ in range(warm):
-        prefill_once()
-    assert kda.kda_check_status(stream) == 0
-
-    # per-kernel timing marks recorded by the library inside every timed step
-    n_marks = 8
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(n_marks)] for _ in range(args.steps)]
-    for evs in marks:
-        for e in evs:
-            e.record(stream)          # create the events before the timed region
-    torch.cuda.synchronize(dev)
-
-    def soak(seconds):
-        """The same step, untimed, back to back for about `seconds`."""
-        t_end = time.perf_counter() + seconds
-        while time.perf_counter() < t_end:
-            for _ in range(8):
-                prefill_once()
-            torch.cuda.synchronize(dev)
-
-    # ---- device-resident timed region.  nvidia-smi samples every 200 ms, far
-    # longer than the timed steps, so the sampler runs over a window in which
-    # the same step keeps the GPU busy: 0.6 s before the timed region (while the
-    # sampler starts), the region itself, and 0.4 s after it.
-    clocks = ClockSampler(dev)
-    clocks.start()
-    soak(0.6)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    recorded = []
-    torch.cuda.synchronize(dev)
-    barrier(dist_on)
-    launches0 = kda.kda_launch_count()
-    ev0.record(stream)
-    for i in range(args.steps):
-        recorded.append(kda.kda_prefill_chunked_events(pargs, marks[i], stream))
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(dist_on)
-    launches = kda.kda_launch_count() - launches0
-    soak(0.4)
-    clk = clocks.stop()
-    clk["window"] = "0.6 s before to 0.4 s after the timed region, the same step running throughout"
-    value, total_ms = replica_throughput(total * args.steps, ev0.elapsed_time(ev1), world, dist_on, dev)
+    # ---- device-resident timed region: the plain entry point, K steps
+    ms_per_step, clk, launches = time_prefill(kda, lib, pargs, stream, dev, args.steps, warm, dist_on)
+    value, total_ms = replica_throughput(total * args.steps, ms_per_step * args.steps, world, dist_on, dev)
     ms_per_step = total_ms / args.steps
-    assert kda.kda_check_status(stream) == 0
-
-    stages = {}
-    for rec in recorded:
-        for (name, e_a), (_, e_b) in zip(rec[:-1], rec[1:]):
-            stages[name] = stages.get(name, 0.0) + e_a.elapsed_time(e_b) / args.steps
-    dom_name, dom_ms = max(stages.items(), key=lambda kv: kv[1])
+    # ---- per-kernel times from a separate pass of the instrumented entry point
+    stages = stage_times(kda, pargs, stream, dev, args.steps)
     th = total * H
-    path_bytes = th * PREFILL_BYTES_PER_TH + n * H * d * d * 4
+    method_bytes = th * PREFILL_BYTES_PER_TH                     # 1796 B per token-head
+    path_bytes = method_bytes + n * H * d * d * 4                # + the final states
     alg_flops = th * PREFILL_FLOPS_PER_TH
-    # the dominant kernel's own algorithmic traffic
-    if dom_name == "chunk_local":
-        n_ch = (T // 64) * n * H
-        dom_bytes = th * (3 * 256 + 512 + 4) + n_ch * CHUNK_RECORD_BYTES
-        dom_note = "reads q, k, v, alpha, beta; writes one 74,240-byte record per (chunk, head)"
-    elif dom_name == "chunk_recur":
-        n_ch = (T // 64) * n * H
-        dom_bytes = n_ch * CHUNK_RECORD_BYTES + th * (256 + 256) + n * H * d * d * 4
-        dom_note = "reads one record per (chunk, head); writes o, snapshots and final states"
-    else:
-        dom_bytes = path_bytes
-        dom_note = "the whole path's algorithmic bytes"
-    fp = kernel_fingerprint()
+    dom_name = max(stages.items(), key=lambda kv: kv[1])[0]
     traffic = RECORDED_TRAFFIC.get((dom_name, kernel_fingerprint(dom_name))) if dom_name in KERNEL_SOURCES else None
-    roofline = {"bound": "hbm", "kernel": dom_name,
-                "achieved": dom_bytes / (dom_ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": dom_bytes / (dom_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                "traffic": traffic, "peak_source": peaks["source"],
-                "algorithmic_bytes_per_launch": dom_bytes, "bytes_counted": dom_note,
-                "ms_per_launch": dom_ms}
+    roofline = roofline_of(stages, method_bytes, peaks, traffic)
+    # the same bytes split by the kernel that must move them, and this design's
+    # own intermediate (the per-(chunk, head) records) reported apart
+    n_items = (T // 64) * n * H
+    per_kernel = {}
+    if "chunk_local" in stages:
+        b = th * (3 * 256 + 512 + 4)
+        per_kernel["chunk_local"] = {"method_bytes": b, "ms": stages["chunk_local"],
+                                     "frac_of_hbm": b / (stages["chunk_local"] / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                     "counts": "q, k, v, alpha, beta"}
+    if "chunk_recur" in stages:
+        b = th * (256 + 256) + n * H * d * d * 4
+        per_kernel["chunk_recur"] = {"method_bytes": b, "ms": stages["chunk_recur"],
+                                     "frac_of_hbm": b / (stages["chunk_recur"] / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                     "counts": "o, snapshots, final states"}
+    roofline["per_kernel"] = per_kernel
+    roofline["design_overhead_bytes_per_step"] = {
+        "value": 2 * n_items * CHUNK_RECORD_BYTES if "chunk_local" in stages else 0,
+        "what": "per-(chunk, head) records written by the chunk-local stage and read back by the carry"}
     path = {"achieved_gbs": path_bytes / (ms_per_step / 1e3) / 1e9,
             "frac_of_hbm": path_bytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"],
             "algorithmic_bytes_per_step": path_bytes,
@@ -343,6 +469,7 @@ def bench_ours(args, rank, world, dev, dist_on):
               "peak_tflops": peaks["bf16_tflops"],
               "frac": alg_flops / (ms_per_step / 1e3) / 1e12 / peaks["bf16_tflops"],
               "algorithmic_flops_per_step": alg_flops}
+    fp = kernel_fingerprint()
 
     # ---- end to end through the C ABI from pinned host buffers
     o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
@@ -579,6 +706,15 @@ def bench_ours(args, rank, world, dev, dist_on):
     copy_bytes = 2 * 2 * gbuf.numel() * 4
     assert kda.kda_check_status(stream) == 0
 
+    # ---- the long-context sequence and the mixed varlen batch, timed the same way
+    extra = {}
+    if not args.no_extra:
+        del dpool, dins, sins, fins, fcpool, gbuf
+        torch.cuda.empty_cache()
+        for name in ("long_1m", "varlen_64"):
+            extra[name] = bench_extra_workload(name, kda, lib, dev, stream, peaks, max(3, min(args.steps, 10)),
+                                               warm, dist_on)
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": warm, "ms_per_step": ms_per_step,
@@ -609,6 +745,7 @@ def bench_ours(args, rank, world, dev, dist_on):
                           "ms_per_step": copy_ms, "states": 128},
         "kernel_fingerprint": fp,
     }
+    line.update(extra)
     if rank == 0:
         line["prefix_cache"] = bench_prefix_cache()
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
@@ -697,6 +834,54 @@ def bench_reference(args, world=1):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_case(args):
+    """One small case for profilers (ncu captures): ``--case prefill`` runs
+    ``--reps`` chunked prefills of ``--seqs`` x ``--len`` tokens, ``--heads``
+    heads, d = ``--dim``, after one warm-up; ``--case decode`` runs decode steps
+    of ``--seqs`` x ``--heads`` states.  Prints the CUDA-event median (not a
+    bench value when run under a profiler)."""
+    import hybrid_linear_attention_kda_gb300 as kda
+    from hybrid_linear_attention_kda_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kda.load()
+    H, d = args.heads, args.dim
+    dt = torch.bfloat16 if args.dtype == "bf16" else torch.float32
+    times = []
+    if args.case == "prefill":
+        lens = [args.len] * args.seqs
+        data = inputs.gen_prefill_device(lens, H, d, d, 20261, dev, dtype=dt, decay=args.decay)
+        pool, table, _ = make_pool_table(lens, [0] * len(lens), H, d, dev)
+        fin = torch.empty((len(lens), H, d, d), device=dev)
+        o = torch.empty((sum(lens), H, d), dtype=dt, device=dev)
+        pargs = kda.make_prefill_args(data["q"], data["k"], data["v"], data["alpha"], data["beta"],
+                                      data["cu_seqlens_dev"], sum(lens), o, pool=pool, snap_table=table,
+                                      final_state=fin)
+        need = kda.kda_prefill_workspace_size(pargs)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        pargs.workspace, pargs.workspace_bytes = ws.data_ptr(), need
+        fn = lambda: kda.kda_prefill_chunked(pargs)  # noqa: E731
+        fn()
+    else:
+        pool = inputs.gen_states(args.seqs, H, d, d, 20263).to(dev)
+        slots = torch.arange(args.seqs, dtype=torch.int32, device=dev)
+        z = {k_: t.to(dev) for k_, t in inputs.gen_decode(args.seqs, H, d, d, 20263, 0, dtype=dt).items()}
+        o = torch.empty((args.seqs, H, d), dtype=dt, device=dev)
+        fn = lambda: kda.kda_decode_step(z["q"], z["k"], z["v"], z["alpha"], z["beta"], pool, slots, o)  # noqa: E731
+        fn()
+    torch.cuda.synchronize()
+    for _ in range(args.reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    assert kda.kda_check_status() == 0
+    print(json.dumps({"case": args.case, "seqs": args.seqs, "len": args.len, "heads": H, "dim": d,
+                      "dtype": args.dtype, "median_ms": statistics.median(times)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -705,7 +890,21 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the 2^20-token and mixed varlen prefill workloads")
+    ap.add_argument("--case", choices=["prefill", "decode"], default=None,
+                    help="run one small case for a profiler instead of the benchmark")
+    ap.add_argument("--seqs", type=int, default=2)
+    ap.add_argument("--len", type=int, default=8192)
+    ap.add_argument("--heads", type=int, default=32)
+    ap.add_argument("--dim", type=int, default=128)
+    ap.add_argument("--dtype", choices=["bf16", "fp32"], default="bf16")
+    ap.add_argument("--decay", choices=["config", "mild"], default="config")
+    ap.add_argument("--reps", type=int, default=2)
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -232,15 +232,7 @@ def gen_varlen_resume(n_seqs, H, d_k, d_v, max_len, prefix_len, n_resume, seed,
     (int32), lens (full lengths), resumed (sorted indices), and ``prefix`` (the
     shared prefix's own tensors, [prefix_len, H, .]).
     """
-    g = _stream(seed, LAYOUT_STREAM)
-    lens = torch.randint(1, max_len + 1, (n_seqs,), generator=g).tolist()
-    eligible = [i for i in range(n_seqs) if lens[i] > interval]
-    perm = torch.randperm(len(eligible), generator=g).tolist()
-    resumed = sorted(eligible[j] for j in perm[:n_resume])
-    start = [0] * n_seqs
-    for i in resumed:
-        m_max = min(prefix_len, lens[i] - 1) // interval
-        start[i] = interval * int(torch.randint(1, m_max + 1, (1,), generator=g))
+    lens, resumed, start = varlen_layout(n_seqs, max_len, prefix_len, n_resume, seed, interval)
 
     prefix = _empty(prefix_len, H, d_k, d_v, dtype)
     _draw_into(_stream(seed, PREFIX_STREAM), prefix_len, H, d_k, d_v, dtype, decay, prefix, 0)
@@ -266,3 +258,85 @@ def gen_varlen_resume(n_seqs, H, d_k, d_v, max_len, prefix_len, n_resume, seed,
     out.update({"cu_seqlens": cu, "start_pos": torch.tensor(start, dtype=torch.int32),
                 "lens": lens, "resumed": resumed, "prefix": prefix})
     return out
+
+
+# ----------------------------------------------------------------------------- device-side draws
+
+def varlen_layout(n_seqs, max_len, prefix_len, n_resume, seed, interval=256):
+    """The layout of the mixed varlen batch of ``gen_varlen_resume``: full lengths,
+    the resumed sequences and their start positions (drawn on the host from the
+    same stream, so both generators agree on it)."""
+    g = _stream(seed, LAYOUT_STREAM)
+    lens = torch.randint(1, max_len + 1, (n_seqs,), generator=g).tolist()
+    eligible = [i for i in range(n_seqs) if lens[i] > interval]
+    perm = torch.randperm(len(eligible), generator=g).tolist()
+    resumed = sorted(eligible[j] for j in perm[:n_resume])
+    start = [0] * n_seqs
+    for i in resumed:
+        m_max = min(prefix_len, lens[i] - 1) // interval
+        start[i] = interval * int(torch.randint(1, m_max + 1, (1,), generator=g))
+    return lens, resumed, start
+
+
+def _device_block(g, n, H, d_k, d_v, decay, device, dtype):
+    """n tokens of the recipe above drawn on ``device`` in float32."""
+    q = torch.randn((n, H, d_k), generator=g, device=device)
+    q = q / torch.linalg.vector_norm(q, dim=-1, keepdim=True)
+    k = torch.randn((n, H, d_k), generator=g, device=device)
+    k = k / torch.linalg.vector_norm(k, dim=-1, keepdim=True)
+    v = torch.randn((n, H, d_v), generator=g, device=device)
+    a = torch.randn((n, H, d_k), generator=g, device=device) + _DECAY_SHIFT[decay]
+    alpha = torch.exp(-torch.nn.functional.softplus(a))
+    beta = torch.sigmoid(torch.randn((n, H), generator=g, device=device))
+    return q.to(dtype), k.to(dtype), v.to(dtype), alpha, beta
+
+
+def gen_prefill_device(seq_lens, H, d_k, d_v, seed, device, dtype=torch.bfloat16, decay="config",
+                       block=65536):
+    """Packed prefill inputs drawn directly on ``device`` by the same recipe, in
+    float32 with a seeded device generator: for timing runs at full size, where
+    drawing gigabytes in float64 on the host would take minutes.  These are not
+    the bytes ``gen_prefill`` produces.  Returns the same dict keys (tensors on
+    ``device``; cu_seqlens on the host and on the device as ``cu_seqlens_dev``)."""
+    seq_lens = [int(x) for x in seq_lens]
+    T = sum(seq_lens)
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + 17)
+    out = {"q": torch.empty((T, H, d_k), dtype=dtype, device=device),
+           "k": torch.empty((T, H, d_k), dtype=dtype, device=device),
+           "v": torch.empty((T, H, d_v), dtype=dtype, device=device),
+           "alpha": torch.empty((T, H, d_k), dtype=torch.float32, device=device),
+           "beta": torch.empty((T, H), dtype=torch.float32, device=device)}
+    for b in range(0, T, block):
+        n = min(block, T - b)
+        for key, t in zip(("q", "k", "v", "alpha", "beta"), _device_block(g, n, H, d_k, d_v, decay, device, dtype)):
+            out[key][b:b + n] = t
+    cu = torch.zeros(len(seq_lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.tensor(np.cumsum(seq_lens), dtype=torch.int32) if seq_lens else cu[1:]
+    out.update({"cu_seqlens": cu, "cu_seqlens_dev": cu.to(device), "seq_lens": seq_lens})
+    return out
+
+
+def gen_varlen_resume_device(n_seqs, H, d_k, d_v, max_len, prefix_len, n_resume, seed, device,
+                             dtype=torch.bfloat16, decay="config", interval=256):
+    """The mixed varlen batch of ``gen_varlen_resume`` (same layout), with its
+    token values drawn on ``device`` as in ``gen_prefill_device``.  Resumed
+    sequences share the prefix's values over their first min(L_i, prefix_len)
+    tokens; only tokens [p_i, L_i) are packed.  Returns the packed tensors,
+    cu_seqlens (host and ``cu_seqlens_dev``), start_pos (host), lens, resumed
+    and ``prefix`` (its own tensors on ``device``)."""
+    lens, resumed, start = varlen_layout(n_seqs, max_len, prefix_len, n_resume, seed, interval)
+    prefix = gen_prefill_device([prefix_len], H, d_k, d_v, seed + 1, device, dtype, decay)
+    packed = [lens[i] - start[i] for i in range(n_seqs)]
+    body = gen_prefill_device(packed, H, d_k, d_v, seed + 2, device, dtype, decay)
+    cu = body["cu_seqlens"].tolist()
+    rs = set(resumed)
+    for i in range(n_seqs):
+        if i in rs:
+            shared = min(lens[i], prefix_len) - start[i]      # packed tokens still inside the prefix
+            if shared > 0:
+                for key in ("q", "k", "v", "alpha", "beta"):
+                    body[key][cu[i]:cu[i] + shared] = prefix[key][start[i]:start[i] + shared]
+    body.update({"start_pos": torch.tensor(start, dtype=torch.int32), "lens": lens, "resumed": resumed,
+                 "prefix": prefix})
+    return body
