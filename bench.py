@@ -129,7 +129,8 @@ class ClockSampler:
 # The sources each prefill kernel is compiled from: its own file and the
 # headers it includes.
 KERNEL_SOURCES = {
-    "chunk_local": ("csrc/chunk_local.cu", "csrc/chunk_common.cuh", "csrc/kda_common.cuh", "csrc/tc05.cuh"),
+    "chunk_local": ("csrc/chunk_local.cu", "csrc/chunk_common.cuh", "csrc/chunk_decay.cuh", "csrc/kda_common.cuh",
+                    "csrc/tc05.cuh"),
     "chunk_recur": ("csrc/chunk_recur.cu", "csrc/chunk_common.cuh", "csrc/kda_common.cuh", "csrc/tc05.cuh"),
 }
 

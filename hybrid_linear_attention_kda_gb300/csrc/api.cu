@@ -113,7 +113,13 @@ kda_status_t validate_prefill(const kda_prefill_args* a) {
 
 size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
 
-bool use_chunked(const kda_prefill_args* a) { return a->dtype == KDA_BF16 && a->d_k == 128; }
+// bf16 with d = 128 runs the tensor-core stages; fp32 q/k/v and d = 64 the same
+// chunk algorithm in fp32 SIMT arithmetic (chunk_simt.cu).
+bool use_tensor_cores(const kda_prefill_args* a) { return a->dtype == KDA_BF16 && a->d_k == 128; }
+
+size_t record_bytes(const kda_prefill_args* a) {
+    return use_tensor_cores(a) ? (size_t)kda::kRecBytes : kda::simt_record_bytes(a->d_k);
+}
 
 // Upper bound on the chunks of a batch: each sequence starts chunk-aligned
 // (start_pos is a multiple of snap_interval), so it has at most one partial chunk.
@@ -126,7 +132,7 @@ int64_t max_chunks_for(const kda_prefill_args* a) {
 // others idle): when the batch has fewer chains than half the SMs and at least
 // two segments' worth of tokens.
 bool split_for(const kda_prefill_args* a) {
-    if (!use_chunked(a) || a->total_tokens < 2 * kda::kSegTokens) return false;
+    if (!use_tensor_cores(a) || a->total_tokens < 2 * kda::kSegTokens) return false;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -139,22 +145,26 @@ int64_t max_segs_for(const kda_prefill_args* a) { return kda::max_segments(a->to
 int64_t max_scratch_for(const kda_prefill_args* a) { return kda::max_segments(a->total_tokens, a->n_seqs); }
 
 struct WorkspaceLayout {
-    size_t chunk_base, chain_flag, chunk_info, records, seg_info, seg_count, seg_state, total;
+    size_t chunk_base, exact_count, exact_items, chunk_info, records, seg_info, seg_count, seg_state, total;
     bool split;
 };
 
 WorkspaceLayout layout_for(const kda_prefill_args* a) {
     WorkspaceLayout w{};
-    if (!use_chunked(a) || a->n_seqs == 0) return w;
+    if (a->n_seqs == 0) return w;
     size_t off = 0;
     w.chunk_base = off;
     off = round_up(off + sizeof(int32_t) * ((size_t)a->n_seqs + 1), 256);
-    w.chain_flag = off;
-    off = round_up(off + sizeof(int32_t) * (size_t)a->n_seqs * a->n_heads, 256);
+    w.exact_count = off;
+    off = round_up(off + sizeof(uint32_t), 256);
+    if (use_tensor_cores(a)) {
+        w.exact_items = off;
+        off = round_up(off + sizeof(int64_t) * (size_t)max_chunks_for(a) * a->n_heads, 256);
+    }
     w.chunk_info = off;
     off = round_up(off + sizeof(int4) * (size_t)max_chunks_for(a), 256);
     w.records = off;
-    off += (size_t)max_chunks_for(a) * a->n_heads * kda::kRecBytes;
+    off += (size_t)max_chunks_for(a) * a->n_heads * record_bytes(a);
     w.split = split_for(a);
     if (w.split) {
         off = round_up(off, 256);
@@ -246,29 +256,19 @@ kda_status_t prefill_impl(const kda_prefill_args* a, void* stream, Marks* m) {
     st = status_ptr(&status);
     if (st != KDA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    kda::PrefillLaunch p;
-    p.a = *a;
-    p.chain_flag = nullptr;
-    p.status = status;
 #define KDA_MARK(name)                          \
     do {                                        \
         kda_status_t ms_ = mark(m, s, name);    \
         if (ms_ != KDA_OK) return ms_;          \
     } while (0)
-    if (!use_chunked(a)) {
-        KDA_MARK("prefill_token");
-        cudaError_t e = kda::launch_prefill_token(p, s);
-        if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-        KDA_MARK("end");
-        return KDA_OK;
-    }
     const WorkspaceLayout w = layout_for(a);
     uint8_t* ws = static_cast<uint8_t*>(a->workspace);
     kda::ChunkLaunch c;
     c.a = *a;
     c.chunk_base = reinterpret_cast<int32_t*>(ws + w.chunk_base);
-    c.chain_flag = reinterpret_cast<int32_t*>(ws + w.chain_flag);
     c.chunk_info = reinterpret_cast<int4*>(ws + w.chunk_info);
+    c.exact_count = reinterpret_cast<uint32_t*>(ws + w.exact_count);
+    c.exact_items = use_tensor_cores(a) ? reinterpret_cast<int64_t*>(ws + w.exact_items) : nullptr;
     c.records = ws + w.records;
     c.max_chunks = max_chunks_for(a);
     c.status = status;
@@ -285,9 +285,22 @@ kda_status_t prefill_impl(const kda_prefill_args* a, void* stream, Marks* m) {
         e = kda::launch_segment_meta(c, s);
         if (e != cudaSuccess) return cuda_fail(e, "prefill segment table launch");
     }
+    if (!use_tensor_cores(a)) {
+        KDA_MARK("simt_local");
+        e = kda::launch_simt_local(c, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill chunk-local (SIMT) launch");
+        KDA_MARK("simt_recur");
+        e = kda::launch_simt_recur(c, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill carry (SIMT) launch");
+        KDA_MARK("end");
+        return KDA_OK;
+    }
     KDA_MARK("chunk_local");
     e = kda::launch_chunk_local(c, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill chunk-local launch");
+    KDA_MARK("chunk_exact");
+    e = kda::launch_chunk_exact(c, s);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill exact-item launch");
     if (w.split) {
         // segment maps A (identity start, U~ = 0) and B (zero start), the scan of
         // the segments' start states, then every segment in parallel
@@ -307,11 +320,6 @@ kda_status_t prefill_impl(const kda_prefill_args* a, void* stream, Marks* m) {
     KDA_MARK("chunk_recur");
     e = kda::launch_chunk_recur(c, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill chunk-recurrence launch");
-    // chains whose gates left the factorisation's range: token by token
-    KDA_MARK("prefill_token_fallback");
-    p.chain_flag = c.chain_flag;
-    e = kda::launch_prefill_token(p, s);
-    if (e != cudaSuccess) return cuda_fail(e, "prefill fallback launch");
     KDA_MARK("end");
 #undef KDA_MARK
     return KDA_OK;

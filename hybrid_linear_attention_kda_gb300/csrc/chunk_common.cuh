@@ -1,4 +1,5 @@
-// Shared definitions of the chunked prefill (d_k = d_v = 128, chunk 64, bf16).
+// Shared definitions of the chunked prefill (chunk 64; the tensor-core stages take
+// bf16 with d_k = d_v = 128, the SIMT stages of chunk_simt.cu the rest).
 //
 // The chunked form ("block-matrix" form of the yunthe.com "Kimi K3 open-source
 // practice" page, FlashKDA paragraph) of the gated delta rule, for a chunk of
@@ -74,9 +75,10 @@ struct ChunkLaunch {
     kda_prefill_args a;
     int32_t* chunk_base;   // [n_seqs + 1]: first chunk of each sequence, total at [n_seqs]
     int4* chunk_info;      // [max_chunks]: {first packed token, tokens (<= 64), sequence, 0}
-    int32_t* chain_flag;   // [n_seqs * H]: nonzero = recompute this (sequence, head) token by token
-    uint8_t* records;      // [max_chunks * H * kRecBytes]
+    uint8_t* records;      // [max_chunks * H] records (kRecBytes each, or simt_record_bytes(d))
     int64_t max_chunks;
+    uint32_t* exact_count;   // items listed in exact_items (zeroed by the meta kernel)
+    int64_t* exact_items;    // [max_chunks * H]: items whose P, W, U~ chunk_exact_kernel rewrites
     uint32_t* status;
     // segments (used when split is set)
     int32_t split;         // nonzero: sequences of >= 2 kSegTokens tokens are split
@@ -116,8 +118,14 @@ __device__ __forceinline__ bool seq_valid(const kda_prefill_args& a, int seq, in
 
 cudaError_t launch_chunk_meta(const ChunkLaunch& p, cudaStream_t s);
 cudaError_t launch_chunk_local(const ChunkLaunch& p, cudaStream_t s);
+cudaError_t launch_chunk_exact(const ChunkLaunch& p, cudaStream_t s);
 cudaError_t launch_chunk_recur(const ChunkLaunch& p, cudaStream_t s);
 cudaError_t launch_segment_meta(const ChunkLaunch& p, cudaStream_t s);
 cudaError_t launch_segment_scan(const ChunkLaunch& p, cudaStream_t s);
+
+// The same two stages in fp32 SIMT arithmetic (chunk_simt.cu): fp32 q/k/v, or d = 64.
+size_t simt_record_bytes(int d);
+cudaError_t launch_simt_local(const ChunkLaunch& p, cudaStream_t s);
+cudaError_t launch_simt_recur(const ChunkLaunch& p, cudaStream_t s);
 
 }  // namespace kda

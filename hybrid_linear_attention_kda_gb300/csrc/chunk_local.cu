@@ -26,13 +26,16 @@
 //                                 cols 64..127  k_r phi_r   -> A (same rows)
 // For r in half 1, phi_r xi_s = exp(g_r - g_s) exactly; where xi_s underflows the
 // true entry is below 2^-100 * e^-87 relative to the others.  Within a half phi,
-// psi span at most 16 tokens; a chunk whose factors leave [2^-100, 2^100] flags
-// its (sequence, head) for the token-serial kernel.  T = (I + A)^-1 is inverted
+// psi span at most 16 tokens; an item whose factors leave [2^-100, 2^100] is
+// listed, and chunk_exact_kernel rewrites its P, W and U~ in fp32 from exact
+// products of alphas (chunk_decay.cuh) before the carry reads them.
+// T = (I + A)^-1 is inverted
 // by 16 x 16 blocks in fp32, then W and U~ come from a second MMA
 // (X^T T'^T and V^T T'^T with X = Gamma K and T' = T diag(beta)).
 #include <cuda.h>
 
 #include "chunk_common.cuh"
+#include "chunk_decay.cuh"
 
 namespace kda {
 namespace {
@@ -458,7 +461,10 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
 
         if (tid == 0) {
             if (ms.guard_fail) {
-                atomicOr(&p.chain_flag[(int64_t)it.seq * H + it.h], 1);
+                // factors outside the operand range: chunk_exact_kernel rewrites
+                // this item's P, W and U~ from exact products of alphas
+                const uint32_t idx = atomicAdd(p.exact_count, 1u);
+                if (idx < (uint64_t)n_items) p.exact_items[idx] = item;
                 ms.guard_fail = 0;
             }
             const uint32_t idesc = idesc_bf16(128, 128, true, true);
@@ -644,17 +650,132 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
+// ---------------------------------------------------------------- exact items
+// Items whose decay factors left the MMA form's operand range get their P, W
+// and U~ tiles rewritten here, in fp32 from exact products of alphas
+// (chunk_decay.cuh): A and P by pairs, T = (I + A)^-1 by forward substitution,
+// W = T diag(beta) (Gamma * K) and U~ = T diag(beta) V, stored in the record's
+// bf16 layout.  Their Q~, Kbar and gamma involve no reference factor and stand
+// as chunk_local_kernel wrote them.
+constexpr int kExactThreads = 256;
+
+struct ExactSmem {
+    float A[64][65];
+    float T[64][65];
+    DecayBlock D;
+    float V[64][kDecayLd];
+    float beta[64];
+};
+
+__device__ __forceinline__ void st_bf16(uint8_t* p, float x) {
+    *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
+}
+
+__global__ void __launch_bounds__(kExactThreads) chunk_exact_kernel(ChunkLaunch p) {
+    extern __shared__ __align__(16) uint8_t exact_smem[];
+    ExactSmem& sm = *reinterpret_cast<ExactSmem*>(exact_smem);
+    const kda_prefill_args& a = p.a;
+    const int H = a.n_heads;
+    const int tid = threadIdx.x;
+    const int64_t total_chunks = p.chunk_base[a.n_seqs] < p.max_chunks ? p.chunk_base[a.n_seqs] : p.max_chunks;
+    const int64_t n_items = total_chunks * H;
+    const uint32_t listed = *p.exact_count;
+    const int64_t count = (int64_t)listed < n_items ? (int64_t)listed : n_items;
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
+    const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
+    DecayBlock& D = sm.D;
+    const int r = tid >> 2, cs = tid & 3;
+    for (int64_t i = blockIdx.x; i < count; i += gridDim.x) {
+        const int64_t item = p.exact_items[i];
+        if (item < 0 || item >= n_items) continue;
+        const int64_t g = item / H;
+        const int h = (int)(item % H);
+        const int4 info = p.chunk_info[g];
+        const int64_t t0 = info.x;
+        const int n = info.y;
+        uint8_t* rec = p.records + (size_t)item * kRecBytes;
+        __syncthreads();
+        if (tid < 64) sm.beta[tid] = tid < n ? a.beta[(t0 + tid) * H + h] : 0.f;
+        float accA[16], accP[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) accA[m] = accP[m] = 0.f;
+        auto load_block = [&](int cb, bool with_q) {
+            __syncthreads();
+            for (int e = tid; e < 64 * kDecayCB; e += kExactThreads) {
+                const int t = e / kDecayCB, c = e % kDecayCB;
+                const bool in = t < n;
+                const size_t off = ((size_t)(t0 + t) * H + h) * kD + cb + c;
+                D.k[t][c] = in ? __bfloat162float(k[off]) : 0.f;
+                D.q[t][c] = in && with_q ? __bfloat162float(q[off]) : 0.f;
+                D.al[t][c] = in ? a.alpha[off] : 1.f;
+                if (!with_q) sm.V[t][c] = in ? __bfloat162float(v[off]) : 0.f;
+            }
+            __syncthreads();
+            decay_tables(D, tid, kExactThreads);
+            __syncthreads();
+        };
+        for (int cb = 0; cb < kD; cb += kDecayCB) {
+            load_block(cb, true);
+            accumulate_ap(D, r, cs, accA, accP);
+        }
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const int s = cs + 4 * m;
+            sm.A[r][s] = s < r ? sm.beta[r] * accA[m] : 0.f;
+            // P tile: row s (key token), column r
+            st_bf16(rec + kRecP + row64_chunk_off(s, r >> 3) + (r & 7) * 2, s <= r ? accP[m] : 0.f);
+        }
+        __syncthreads();
+        if (tid < 64) {                       // T = (I + A)^-1, column j per thread
+            const int j = tid;
+            for (int x = 0; x < j; ++x) sm.T[x][j] = 0.f;
+            sm.T[j][j] = 1.f;
+            for (int x = j + 1; x < 64; ++x) {
+                float acc = 0.f;
+                for (int s = j; s < x; ++s) acc = fmaf(sm.A[x][s], sm.T[s][j], acc);
+                sm.T[x][j] = -acc;
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < 64 * 64; e += kExactThreads) sm.T[e >> 6][e & 63] *= sm.beta[e & 63];
+        // W_tc = sum_s T'_ts Gamma_sc k_sc and U~_tj = sum_s T'_ts v_sj, 16 channels at a time
+        for (int cb = 0; cb < kD; cb += kDecayCB) {
+            load_block(cb, false);
+            for (int e = tid; e < 64 * kDecayCB; e += kExactThreads) {   // X = Gamma * K over k
+                const int t = e / kDecayCB, c = e % kDecayCB;
+                D.q[t][c] = prefix_decay(D, t, c) * D.k[t][c];
+            }
+            __syncthreads();
+            for (int e = tid; e < 64 * kDecayCB; e += kExactThreads) {
+                const int t = e % 64, c = e / 64;
+                float w = 0.f, u = 0.f;
+                for (int s = 0; s <= t; ++s) {
+                    const float tt = sm.T[t][s];
+                    w = fmaf(tt, D.q[s][c], w);
+                    u = fmaf(tt, sm.V[s][c], u);
+                }
+                const uint32_t off = row64_chunk_off(cb + c, t >> 3) + (t & 7) * 2;
+                st_bf16(rec + kRecW + off, w);
+                st_bf16(rec + kRecU + off, u);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- meta: chunk table
 // chunk_base[s] = first global chunk of sequence s (exclusive scan of
-// ceil(L_s / 64) over valid sequences); chain flags cleared.
+// ceil(L_s / 64) over valid sequences).
 __global__ void __launch_bounds__(1024) chunk_meta_kernel(ChunkLaunch p) {
     const kda_prefill_args& a = p.a;
-    const int n = a.n_seqs, H = a.n_heads;
+    const int n = a.n_seqs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __shared__ int64_t warp_tot[32];
     __shared__ int64_t carry;
-    for (int64_t i = tid; i < (int64_t)n * H; i += blockDim.x) p.chain_flag[i] = 0;
-    if (tid == 0) carry = 0;
+    if (tid == 0) {
+        carry = 0;
+        *p.exact_count = 0;
+    }
     __syncthreads();
     for (int base = 0; base < n; base += 1024) {
         const int s = base + tid;
@@ -716,6 +837,23 @@ __global__ void __launch_bounds__(1024) chunk_meta_kernel(ChunkLaunch p) {
 }
 
 }  // namespace
+
+cudaError_t launch_chunk_exact(const ChunkLaunch& p, cudaStream_t s) {
+    const int64_t max_items = p.max_chunks * p.a.n_heads;
+    if (max_items == 0 || p.a.total_tokens == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const size_t smem = sizeof(ExactSmem);
+    e = cudaFuncSetAttribute(chunk_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = max_items < 2 * (int64_t)sms ? max_items : 2 * (int64_t)sms;
+    note_launch();
+    chunk_exact_kernel<<<(unsigned)grid, kExactThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_chunk_meta(const ChunkLaunch& p, cudaStream_t s) {
     note_launch();

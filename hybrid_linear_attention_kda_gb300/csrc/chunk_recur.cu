@@ -86,7 +86,6 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     int32_t init;
     uint32_t bad;
     if (!seq_valid(a, seq, &tb, &te, &pos0, &init, &bad)) return;     // flagged by the meta kernel
-    if (p.chain_flag[(int64_t)seq * H + h]) return;                    // recomputed token by token
     const int64_t g_seq = p.chunk_base[seq];
     const int64_t nc_seq = p.chunk_base[seq + 1] - g_seq;
     if (nc_seq < 0 || g_seq + nc_seq > p.max_chunks) return;
@@ -453,7 +452,6 @@ __global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(ChunkLaunch 
     const int tid = threadIdx.x;
     const int32_t s0 = p.seg_count[1 + seq], s1 = p.seg_count[2 + seq];
     if (s1 - s0 < 1 || p.seg_info[s0].w < 0) return;          // not split
-    if (p.chain_flag[(int64_t)seq * H + h]) return;
     int64_t tb, te, pos0;
     int32_t init;
     uint32_t bad;

@@ -1,0 +1,281 @@
+// The chunked prefill in fp32 SIMT arithmetic, for the inputs the tensor-core
+// kernels do not take: fp32 q/k/v (whose 1e-4 accuracy bf16 operands cannot
+// reach) and d_k = d_v = 64.  It is the same algorithm as the tensor-core pair
+// (the block-matrix form of the yunthe.com "Kimi K3 open-source practice" page,
+// FlashKDA paragraph) on the same chunk table: a chunk-local kernel writes one
+// record per (chunk, head), a carry kernel takes the fp32 state of each
+// (sequence, head) through its chunks, with snapshots every 256 absolute
+// positions ("Kimi K3 Tech Intro", sections 2.2-2.4) and resume.
+//
+// For a chunk of n <= 64 tokens r entering with state S (d x d), with the
+// decay factor f_rsc = prod_{s < tau <= r} alpha_tau,c (chunk_decay.cuh) and
+// Gamma_r = prod_{tau <= r} alpha_tau per channel:
+//   A_rs = beta_r sum_c k_rc k_sc f_rsc   (s < r),   P_rs = sum_c q_rc k_sc f_rsc   (s <= r)
+//   T = (I + A)^-1,  T' = T diag(beta)
+//   W = T' (Gamma * K),  U~ = T' V,  Q~ = Gamma * Q,
+//   Kbar_s = (prod_{tau > s} alpha_tau) k_s,  gamma = Gamma_{n-1}
+// the carry is  U = U~ - W S,  O = Q~ S + P U,  S <- Diag(gamma) S + Kbar^T U.
+// Every factor is a product of alphas, so nothing overflows and an underflow is
+// the true (negligible) value.
+//
+// Record of one (chunk, head), fp32, token-major rows:
+//   W [64][D], Q~ [64][D], Kbar [64][D], U~ [64][D], P [64][64], gamma [D]
+#include "chunk_common.cuh"
+#include "chunk_decay.cuh"
+
+namespace kda {
+
+size_t simt_record_bytes(int d) { return (size_t)(4 * 64 * d + 64 * 64 + d) * sizeof(float); }
+
+namespace {
+
+constexpr int kSimtThreads = 256;
+constexpr int kCB = kDecayCB;            // channels per block in the chunk-local passes
+constexpr int kLd = kDecayLd;
+
+template <int D>
+struct SimtRec {
+    static constexpr size_t W = 0, Q = 64 * D, K = 2 * 64 * D, U = 3 * 64 * D, P = 4 * 64 * D;
+    static constexpr size_t G = 4 * 64 * D + 64 * 64;
+    static constexpr size_t floats = G + D;
+};
+
+// Shared memory of the chunk-local kernel (dynamic).
+struct LocalSmem {
+    float A[64][65];          // A (strictly lower, beta_r scaled)
+    float T[64][65];          // T, then T' = T diag(beta)
+    union {
+        DecayBlock p1;        // pass 1: one block of channels
+        struct {              // pass 2
+            float X[64][kLd], V[64][kLd];
+        } p2;
+    } u;
+    float beta[64];
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kSimtThreads) simt_local_kernel(ChunkLaunch p) {
+    using R = SimtRec<D>;
+    extern __shared__ __align__(16) uint8_t simt_smem[];
+    LocalSmem& sm = *reinterpret_cast<LocalSmem*>(simt_smem);
+    const kda_prefill_args& a = p.a;
+    const int H = a.n_heads;
+    const int tid = threadIdx.x;
+    const int64_t total_chunks = p.chunk_base[a.n_seqs] < p.max_chunks ? p.chunk_base[a.n_seqs] : p.max_chunks;
+    const int64_t item = blockIdx.x;
+    if (item >= total_chunks * H) return;
+    const int64_t g = item / H;
+    const int h = (int)(item % H);
+    const int4 info = p.chunk_info[g];
+    const int64_t t0 = info.x;
+    const int n = info.y;
+    float* rec = reinterpret_cast<float*>(p.records) + (size_t)item * R::floats;
+
+    const T* q = static_cast<const T*>(a.q);
+    const T* k = static_cast<const T*>(a.k);
+    const T* v = static_cast<const T*>(a.v);
+    if (tid < 64) sm.beta[tid] = tid < n ? a.beta[(t0 + tid) * H + h] : 0.f;
+
+    // this thread's 16 (r, s) pairs: row r, columns s = cs + 4 m
+    const int r = tid >> 2, cs = tid & 3;
+    float accA[16], accP[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) accA[m] = accP[m] = 0.f;
+
+    // ---------------------------------------------------------------- pass 1
+    DecayBlock& D1 = sm.u.p1;
+    for (int cb = 0; cb < D; cb += kCB) {
+        __syncthreads();
+        for (int e = tid; e < 64 * kCB; e += kSimtThreads) {
+            const int t = e / kCB, c = e % kCB;
+            const bool in = t < n;
+            const size_t off = ((size_t)(t0 + t) * H + h) * D + cb + c;
+            D1.k[t][c] = in ? Elem<T>::load(k + off) : 0.f;
+            D1.q[t][c] = in ? Elem<T>::load(q + off) : 0.f;
+            D1.al[t][c] = in ? a.alpha[off] : 1.f;
+        }
+        __syncthreads();
+        decay_tables(D1, tid, kSimtThreads);
+        __syncthreads();
+        // Q~, Kbar, gamma and (for the second pass) X = Gamma * K into the record
+        for (int e = tid; e < 64 * kCB; e += kSimtThreads) {
+            const int t = e / kCB, c = e % kCB;
+            const float G = prefix_decay(D1, t, c);
+            rec[R::Q + t * D + cb + c] = G * D1.q[t][c];
+            rec[R::K + t * D + cb + c] = suffix_decay(D1, t, c) * D1.k[t][c];
+            rec[R::W + t * D + cb + c] = G * D1.k[t][c];
+            if (t == 63) rec[R::G + cb + c] = G;
+        }
+        accumulate_ap(D1, r, cs, accA, accP);
+    }
+    // A (strictly lower, beta_r scaled) to shared memory; P to the record
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const int s = cs + 4 * m;
+        sm.A[r][s] = s < r ? sm.beta[r] * accA[m] : 0.f;
+        rec[R::P + r * 64 + s] = s <= r ? accP[m] : 0.f;
+    }
+    __syncthreads();
+    // T = (I + A)^-1 by forward substitution, one column j per thread
+    if (tid < 64) {
+        const int j = tid;
+        for (int i = 0; i < j; ++i) sm.T[i][j] = 0.f;
+        sm.T[j][j] = 1.f;
+        for (int i = j + 1; i < 64; ++i) {
+            float acc = 0.f;
+            for (int s = j; s < i; ++s) acc = fmaf(sm.A[i][s], sm.T[s][j], acc);
+            sm.T[i][j] = -acc;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < 64 * 64; e += kSimtThreads) sm.T[e >> 6][e & 63] *= sm.beta[e & 63];
+
+    // ---------------------------------------------------------------- pass 2
+    // W = T' X and U~ = T' V, one block of channels at a time; the block of X
+    // is read from the record's W rows before W overwrites them
+    const int orow = tid >> 2, oc = (tid & 3) * 4;      // 4 outputs of one row per thread
+    for (int cb = 0; cb < D; cb += kCB) {
+        __syncthreads();
+        for (int e = tid; e < 64 * kCB; e += kSimtThreads) {
+            const int t = e / kCB, c = e % kCB;
+            sm.u.p2.X[t][c] = rec[R::W + t * D + cb + c];
+            sm.u.p2.V[t][c] = t < n ? Elem<T>::load(v + ((size_t)(t0 + t) * H + h) * D + cb + c) : 0.f;
+        }
+        __syncthreads();
+        float w4[4] = {0.f, 0.f, 0.f, 0.f}, u4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s = 0; s <= orow; ++s) {
+            const float t = sm.T[orow][s];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                w4[i] = fmaf(t, sm.u.p2.X[s][oc + i], w4[i]);
+                u4[i] = fmaf(t, sm.u.p2.V[s][oc + i], u4[i]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            rec[R::W + orow * D + cb + oc + i] = w4[i];
+            rec[R::U + orow * D + cb + oc + i] = u4[i];
+        }
+    }
+}
+
+// The carry of one (sequence, head): the fp32 state S [D][D] in shared memory.
+template <typename T, int D>
+__global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p) {
+    using R = SimtRec<D>;
+    constexpr int G = kSimtThreads / D;      // thread groups over the second index
+    extern __shared__ __align__(16) uint8_t simt_smem[];
+    float* S = reinterpret_cast<float*>(simt_smem);          // [D][D]
+    float* U = S + D * D;                                    // [64][D]
+    const kda_prefill_args& a = p.a;
+    const int H = a.n_heads;
+    const int tid = threadIdx.x;
+    const int seq = (int)(blockIdx.x / H), h = (int)(blockIdx.x % H);
+    int64_t tb, te, pos0;
+    int32_t init;
+    uint32_t bad;
+    if (!seq_valid(a, seq, &tb, &te, &pos0, &init, &bad)) return;     // flagged by the meta kernel
+    const int64_t g0 = p.chunk_base[seq];
+    const int64_t nc = p.chunk_base[seq + 1] - g0;
+    if (nc < 0 || g0 + nc > p.max_chunks) return;
+    const int64_t slot_stride = (int64_t)H * D * D;
+    const int64_t head_off = (int64_t)h * D * D;
+    const int j = tid % D, grp = tid / D;
+
+    const float* S0 = init >= 0 ? a.pool + (int64_t)init * slot_stride + head_off : nullptr;
+    for (int e = tid; e < D * D; e += kSimtThreads) S[e] = S0 ? S0[e] : 0.f;
+    T* o = static_cast<T*>(a.o);
+
+    for (int64_t lc = 0; lc < nc; ++lc) {
+        const int64_t t0 = tb + lc * kC;
+        const int n = (int)(te - t0 < kC ? te - t0 : kC);
+        const float* rec = reinterpret_cast<const float*>(p.records) + (size_t)((g0 + lc) * H + h) * R::floats;
+        __syncthreads();                                         // S complete
+        // U = U~ - W S
+        for (int t = grp; t < n; t += G) {
+            const float* w = rec + R::W + t * D;
+            float acc = rec[R::U + t * D + j];
+            for (int c = 0; c < D; ++c) acc = fmaf(-w[c], S[c * D + j], acc);
+            U[t * D + j] = acc;
+        }
+        __syncthreads();
+        // O = Q~ S + P U
+        for (int t = grp; t < n; t += G) {
+            const float* qt = rec + R::Q + t * D;
+            const float* pt = rec + R::P + t * 64;
+            float acc = 0.f;
+            for (int c = 0; c < D; ++c) acc = fmaf(qt[c], S[c * D + j], acc);
+            for (int s = 0; s <= t; ++s) acc = fmaf(pt[s], U[s * D + j], acc);
+            Elem<T>::store(o + ((t0 + t) * H + h) * D + j, a.scale * acc);
+        }
+        __syncthreads();                                         // every read of S done
+        // S <- Diag(gamma) S + Kbar^T U
+        for (int c = grp; c < D; c += G) {
+            float acc = rec[R::G + c] * S[c * D + j];
+            for (int t = 0; t < n; ++t) acc = fmaf(rec[R::K + t * D + c], U[t * D + j], acc);
+            S[c * D + j] = acc;
+        }
+        // a snapshot after this chunk
+        const int64_t p_end = pos0 + lc * kC + n;
+        if (a.snap_table && p_end % a.snap_interval == 0) {
+            const int64_t ord = p_end / a.snap_interval - 1;
+            int32_t slot = -1;
+            if (ord >= a.snap_table_stride) {
+                if (tid == 0) flag(p.status, KDA_DEV_BAD_ORDINAL);
+            } else {
+                slot = a.snap_table[(int64_t)seq * a.snap_table_stride + ord];
+                if (slot != -1 && (slot < 0 || (int64_t)slot >= a.n_slots)) {
+                    if (tid == 0) flag(p.status, KDA_DEV_BAD_SLOT);
+                    slot = -1;
+                }
+            }
+            if (slot >= 0) {
+                __syncthreads();
+                float* dst = a.pool + (int64_t)slot * slot_stride + head_off;
+                for (int e = tid; e < D * D; e += kSimtThreads) dst[e] = S[e];
+            }
+        }
+    }
+    __syncthreads();
+    if (a.final_state) {
+        float* dst = a.final_state + (int64_t)seq * slot_stride + head_off;
+        for (int e = tid; e < D * D; e += kSimtThreads) dst[e] = S[e];
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_simt_pair(const ChunkLaunch& p, cudaStream_t s, bool local) {
+    if (local) {
+        const int64_t items = p.max_chunks * p.a.n_heads;
+        if (items == 0 || p.a.total_tokens == 0) return cudaSuccess;
+        const size_t smem = sizeof(LocalSmem);
+        cudaError_t e = cudaFuncSetAttribute(simt_local_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        note_launch();
+        simt_local_kernel<T, D><<<(unsigned)items, kSimtThreads, smem, s>>>(p);
+        return cudaGetLastError();
+    }
+    const int64_t chains = (int64_t)p.a.n_seqs * p.a.n_heads;
+    if (chains == 0) return cudaSuccess;
+    const size_t smem = (size_t)(D * D + 64 * D) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(simt_recur_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    note_launch();
+    simt_recur_kernel<T, D><<<(unsigned)chains, kSimtThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_simt(const ChunkLaunch& p, cudaStream_t s, bool local) {
+    const bool f32 = p.a.dtype == KDA_FP32;
+    if (p.a.d_k == 64) return f32 ? launch_simt_pair<float, 64>(p, s, local) : launch_simt_pair<__nv_bfloat16, 64>(p, s, local);
+    return f32 ? launch_simt_pair<float, 128>(p, s, local) : launch_simt_pair<__nv_bfloat16, 128>(p, s, local);
+}
+
+}  // namespace
+
+cudaError_t launch_simt_local(const ChunkLaunch& p, cudaStream_t s) { return launch_simt(p, s, true); }
+cudaError_t launch_simt_recur(const ChunkLaunch& p, cudaStream_t s) { return launch_simt(p, s, false); }
+
+}  // namespace kda

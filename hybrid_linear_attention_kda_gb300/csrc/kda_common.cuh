@@ -40,14 +40,6 @@ kda_status_t record_error(kda_status_t status, const char* message);
 // Each returns the cudaError_t of its launch.  Arguments were validated by the
 // C-ABI layer.
 
-struct PrefillLaunch {
-    kda_prefill_args a;
-    const int32_t* chain_flag;  // [n_seqs * H] or NULL: when set, only flagged (seq, head) run
-    uint32_t* status;           // device status word
-};
-
-cudaError_t launch_prefill_token(const PrefillLaunch& p, cudaStream_t s);
-
 struct DecodeLaunch {
     int32_t n_seqs, H, D, dtype;
     const void *q, *k, *v;

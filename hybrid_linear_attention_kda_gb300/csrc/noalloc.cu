@@ -16,8 +16,9 @@
 // array, so calls that overlap on the GPU (different streams or threads, without
 // ordering between them) race on it; it keeps the last call's contents.  Every
 // part of it that a call relies on is written by that call's own kernels before
-// it is read (the chunk table and the fallback flags are rewritten by the first
-// kernel), so nothing needs clearing between calls.
+// it is read (the chunk table and the count of listed exact items are rewritten
+// by the first kernel, every record by the chunk-local stage before the carry
+// reads it), so nothing needs clearing between calls.
 //
 // In host code the array's name is only a stand-in for the device variable; the
 // device address comes from cudaGetSymbolAddress, looked up on the first call on

@@ -32,9 +32,11 @@
  *    q, k, v, o share one element type (kda_dtype_t).  Device pointers must be
  *    16-byte aligned.
  *  - Supported shapes: d_k == d_v in {64, 128}; chunk == 64; snap_interval == 256.
- *    Anything else returns KDA_ERR_UNSUPPORTED.  bf16 inputs with d = 128 take
- *    the chunked tensor-core path; fp32 inputs and d = 64 are evaluated token by
- *    token with the fp32 state in registers (same results within rounding).
+ *    Anything else returns KDA_ERR_UNSUPPORTED.  Every prefill runs the chunked
+ *    form (the block-matrix form of the yunthe.com "Kimi K3 open-source
+ *    practice" page, FlashKDA paragraph): bf16 inputs with d = 128 on tensor
+ *    cores (bf16 operands, fp32 accumulation and fp32 state), fp32 inputs and
+ *    d = 64 with the same chunk algorithm in fp32 SIMT arithmetic.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream) and run on the current CUDA device.  Argument errors that
  *    the host can see come back synchronously, before anything is launched.  A
@@ -110,6 +112,12 @@ typedef enum {
  *
  * Chunks are aligned to absolute multiples of `chunk`, and every reduction has
  * a fixed order, so a resumed run reproduces a full run bit for bit.
+ *
+ * The workspace holds the chunk table and one record per (chunk, head) between
+ * the chunk-local stage and the state carry: 74,240 bytes on the tensor-core
+ * path, (4 * 64 * d + 64 * 64 + d) * 4 bytes on the fp32 SIMT path, for at most
+ * total_tokens / 64 + n_seqs chunks.  kda_prefill_workspace_size gives the
+ * exact figure; it is 0 only for an empty batch or invalid sizes.
  */
 typedef struct kda_prefill_args {
     int32_t n_seqs;            /* >= 0 */
@@ -167,10 +175,13 @@ kda_status_t kda_prefill_chunked_events(const kda_prefill_args *args, void *stre
  * pages describe no counterpart to this call; it exists for serving code whose device
  * memory is all reserved up front, or that may not allocate on its latency
  * path.  Allocates nothing.  Returns KDA_ERR_UNSUPPORTED when
- * kda_prefill_workspace_size(args) exceeds 64 MiB.  All calls share the array:
- * calls that overlap on the GPU race on it.  The first call on a device looks up
- * the array's device address (cudaGetSymbolAddress) and should come before any
- * stream capture.
+ * kda_prefill_workspace_size(args) exceeds 64 MiB.  In practice that is about
+ * 900 (chunk, head) records on the bf16, d = 128 path (74,240 bytes each, for
+ * total_tokens / 64 + n_seqs chunks times H heads): for example one 7,000-token
+ * sequence with 8 heads, or 1,700 tokens with 32 heads.  The fp32 SIMT path's
+ * records are twice as large.  All calls share the array: calls that overlap on
+ * the GPU race on it.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) and should come before any stream capture.
  */
 kda_status_t kda_prefill_chunked_noalloc(const kda_prefill_args *args, void *stream);
 

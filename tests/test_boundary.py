@@ -148,9 +148,13 @@ def test_workspace_size_is_zero_for_invalid_sizes(lib):
                  dict(dtype=7), dict(chunk=32), dict(snap_interval=128), dict(total_tokens=-64),
                  dict(total_tokens=1 << 31), dict(n_seqs=-1), dict(n_seqs=(1 << 20) + 1)):
         assert kda.kda_prefill_workspace_size(_args(**over)) == 0, over
-    # the token path (fp32, or d = 64) needs no workspace
-    assert kda.kda_prefill_workspace_size(_args(dtype=kda.KDA_FP32)) == 0
-    assert kda.kda_prefill_workspace_size(_args(d_k=64, d_v=64)) == 0
+    # every dtype and head size runs the chunked stages, so each needs a workspace:
+    # the fp32 SIMT records (4 x 64 x d + 64 x 64 + d floats per (chunk, head))
+    # are larger than the bf16 tensor-core records (74,240 bytes)
+    bf = kda.kda_prefill_workspace_size(_args())
+    f32 = kda.kda_prefill_workspace_size(_args(dtype=kda.KDA_FP32))
+    d64 = kda.kda_prefill_workspace_size(_args(d_k=64, d_v=64))
+    assert f32 > bf > 0 and d64 > 0
 
 
 def test_fused_decode_args_struct_and_checks(lib):

@@ -169,7 +169,9 @@ def test_resume_is_bit_exact_against_the_full_run(kda, cuda_device, dtype):
 
 
 def test_pathological_gates(kda, cuda_device):
-    """alpha exactly 1, alpha down to 1e-30, beta 0 and 1, in runs of tokens."""
+    """alpha exactly 1, alpha down to 1e-30 and exactly 0, beta 0 and 1, in runs
+    of tokens: the chunks whose decay factors leave the tensor-core operand range
+    are rewritten from exact products of alphas."""
     dev = cuda_device
     T, H, d = 333, 2, 128
     data = inputs.gen_prefill([T], H, d, d, 53, dtype=torch.bfloat16)
@@ -178,6 +180,7 @@ def test_pathological_gates(kda, cuda_device):
     a[50:90, :, :17] = 1e-30
     a[100:140] = 1e-12
     a[200:230, 1] = 0.999999
+    a[260:262, 0, 40:48] = 0.0          # outside (0, 1): a hard reset of those channels
     b = data["beta"]
     b[20:30] = 0.0
     b[150:170] = 1.0
@@ -486,9 +489,10 @@ def test_split_and_plain_sequences_in_one_batch(kda, cuda_device):
 
 @pytest.mark.parametrize("dtype, d", [(torch.bfloat16, 128), (torch.float32, 128), (torch.bfloat16, 64)])
 def test_all_empty_batch_writes_the_initial_states(kda, cuda_device, dtype, d):
-    """Three empty sequences (total_tokens = 0) on the chunked path (bf16,
-    d = 128) and the token path: nothing to compute, but every final state is
-    written: zeros without an initial slot, the slot's state when resumed."""
+    """Three empty sequences (total_tokens = 0) on the tensor-core stages (bf16,
+    d = 128) and the SIMT stages (fp32, or d = 64): nothing to compute, but every
+    final state is written: zeros without an initial slot, the slot's state when
+    resumed."""
     dev = cuda_device
     H = 4
     data = inputs.gen_prefill([0, 0, 0], H, d, d, 20272, dtype=dtype)
