@@ -49,6 +49,7 @@ struct Misc {
     uint64_t bar_snapfree;  // output group: staged snapshot written out (128 arrivals)
     uint32_t tslot;
     int32_t failed;
+    int32_t map_stop;       // segment map: the state became exactly zero, so stays zero
 };
 
 static_assert(sizeof(Misc) <= 128, "barrier block");
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         mbar_init(&ms.bar_snap, 32 * kStateWarps);
         mbar_init(&ms.bar_snapfree, 32 * kOutWarps);
         ms.failed = 0;
+        ms.map_stop = 0;
         fence_mbar_init();
     }
     fence_before_sync();
@@ -195,19 +197,22 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
                              id128mn, ks > 0 ? 1u : 0u);
                 mma_commit(&ms.bar_ab);
             };
+            // (d): D3 = U^T Kbar, on the state chain; then (c): D2 += U^T P^T,
+            // which runs while the state group updates S
             auto issue_dc = [&](int64_t lc) {
                 const uint32_t stage = s_base + stage_of(lc);
 #pragma unroll
                 for (int ks = 0; ks < kC / 16; ++ks)
                     mma_bf16(tD3, at(dUa, ks * 32), at(dKM, stage + kRecK + ks * 32), id128, ks > 0 ? 1u : 0u);
                 mma_commit(&ms.bar_d);
+                if (!writes_out) return;            // the map / offset passes need no outputs
 #pragma unroll
                 for (int ks = 0; ks < kC / 16; ++ks)
                     mma_bf16(tD2(lc), at(dUa, ks * 32), at(dMN, stage + kRecP + ks * 2048), id64, 1u);
                 mma_commit(&ms.bar_c);
                 n_c += 1;
             };
-            bool ok = true;
+            bool ok = true, stopped = false;
             if (nc > 0) {
                 load(0);
                 if (nc > 1) load(1);
@@ -220,12 +225,19 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
                 // D2 of lc-1 read by the output group.  Waiting here, before (c) of
                 // lc is issued, keeps that barrier at most one phase ahead of this
                 // wait; the buffer is reused by (ab) of lc+1.
-                if (lc >= 1 && !(ok = waitb(&ms.bar_o, par ^ 1))) break;
+                if (writes_out && lc >= 1 && !(ok = waitb(&ms.bar_o, par ^ 1))) break;
                 fence_after_sync();
                 issue_dc(lc);
                 if (!(ok = waitb(&ms.bar_s, par ^ 1))) break;      // state after lc written
-                if (!(ok = waitb(&ms.bar_c, par))) break;          // every MMA of lc done
-                w_c += 1;
+                // every MMA of lc done: the state group has consumed (ab) and (d);
+                // (c) runs only when outputs are written
+                if (writes_out) {
+                    if (!(ok = waitb(&ms.bar_c, par))) break;
+                    w_c += 1;
+                } else if (mode == kCarryMap && ms.map_stop) {
+                    stopped = true;                                 // the map is zero from here on
+                    break;
+                }
                 fence_after_sync();
                 if (lc + 2 < nc) load(lc + 2);                      // record stage of lc is free
                 if (lc + 1 < nc) {
@@ -233,11 +245,13 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
                     issue_ab(lc + 1);
                 }
             }
-            if (!ok) {
-                // let this CTA's own copies and MMAs land (bounded) before
-                // shared and tensor memory are released
+            if (!ok || stopped) {
+                // let this CTA's own copies (and, on a failure, MMAs) land
+                // (bounded) before shared and tensor memory are released
                 for (int st = 0; st < 2; ++st)
                     for (uint32_t l = ld_waited[st]; l < ld_issued[st]; ++l) mbar_wait(&ms.bar_load[st], l & 1);
+            }
+            if (!ok) {
                 for (uint32_t m = w_c; m < n_c; ++m) mbar_wait(&ms.bar_c, m & 1);
             }
         }
@@ -317,7 +331,28 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
                     S[16 * q4 + e] = fmaf(gam[16 * q4 + e], S[16 * q4 + e], __uint_as_float(v[e]));
             }
             fence_before_sync();
+            // the segment map: once the state is exactly zero every later chunk
+            // keeps it zero, so the map of the whole segment is zero and the pass
+            // stops (an AND over the 256 state threads at named barrier 3)
+            bool map_zero = false;
+            if (mode == kCarryMap) {
+                uint32_t z = 1;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) z &= S[i] == 0.f ? 1u : 0u;
+                uint32_t all;
+                asm volatile(
+                    "{\n\t.reg .pred p, q;\n\t"
+                    "setp.ne.u32 p, %1, 0;\n\t"
+                    "bar.red.and.pred q, 3, 256, p;\n\t"
+                    "selp.u32 %0, 1, 0, q;\n\t}"
+                    : "=r"(all)
+                    : "r"(z)
+                    : "memory");
+                map_zero = all != 0;
+                if (map_zero && tid == 0) ms.map_stop = 1;
+            }
             write_sa();
+            if (map_zero) break;
             // snapshot after this chunk: the fp32 state goes to the snapshot
             // columns of TMEM (lane j, column c); the output group writes it to
             // the pool, off this chain
@@ -354,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
         const int64_t ostride = (int64_t)H * kD;
         uint32_t n_snap = 0;
-        for (int64_t lc = 0; lc < nc; ++lc) {
+        // the map and offset passes write no outputs: (c) is not issued there
+        for (int64_t lc = 0; lc < nc && writes_out; ++lc) {
             if (!waitb(&ms.bar_c, (uint32_t)(lc & 1))) break;
             fence_after_sync();
             uint32_t v[4][16];
@@ -441,14 +477,20 @@ __global__ void segment_meta_kernel(ChunkLaunch p) {
 // Initial states of the segments of one (sequence, head):
 //   S_in(0) = the sequence's initial state,  S_in(k) = A_{k-1} S_in(k-1) + B_{k-1}
 // in fp32, with the snapshot at each segment boundary taken from S_in (the
-// state the next segment continues from).
+// state the next segment continues from).  Each value column of S evolves on
+// its own, so a CTA takes one block of kScanCols columns of one (sequence, head);
+// each step stages A_{k-1} in shared memory.
 constexpr int kScanThreads = 256;
+constexpr int kScanCols = 16;
+constexpr int kScanBlocks = kD / kScanCols;
 
 __global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(ChunkLaunch p) {
     extern __shared__ float scan_smem[];
     const kda_prefill_args& a = p.a;
     const int H = a.n_heads;
-    const int seq = (int)(blockIdx.x / H), h = (int)(blockIdx.x % H);
+    const int64_t sh = blockIdx.x / kScanBlocks;
+    const int cb = (int)(blockIdx.x % kScanBlocks) * kScanCols;     // first column of this block
+    const int seq = (int)(sh / H), h = (int)(sh % H);
     const int tid = threadIdx.x;
     const int32_t s0 = p.seg_count[1 + seq], s1 = p.seg_count[2 + seq];
     if (s1 - s0 < 1 || p.seg_info[s0].w < 0) return;          // not split
@@ -457,44 +499,48 @@ __global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(ChunkLaunch 
     uint32_t bad;
     if (!seq_valid(a, seq, &tb, &te, &pos0, &init, &bad)) return;
     constexpr int DD = kD * kD;
-    float* Scur = scan_smem;
-    float* Snew = scan_smem + DD;
-    float* Am = scan_smem + 2 * DD;
+    float* Am = scan_smem;                                       // [kD][kD + 4]
+    constexpr int kLdA = kD + 4;
+    float* Scur = scan_smem + kD * kLdA;                         // [kD][kScanCols]
     const int64_t head_off = (int64_t)h * DD;
     auto seg_state = [&](int32_t scr, int which) { return p.seg_state + ((int64_t)scr * H * 3 + (int64_t)h * 3 + which) * DD; };
+    const int j = tid % kScanCols, rg = tid / kScanCols;         // column j, rows rg + 16 m
     {
         const float* S0 = init >= 0 ? a.pool + (int64_t)init * H * DD + head_off : nullptr;
         float* dst = seg_state(p.seg_info[s0].w, 2);
-        for (int e = tid; e < DD; e += kScanThreads) {
-            const float x = S0 ? S0[e] : 0.f;
-            Scur[e] = x;
-            dst[e] = x;
+#pragma unroll
+        for (int m = 0; m < kD / 16; ++m) {
+            const int c = rg + 16 * m;
+            const float x = S0 ? S0[c * kD + cb + j] : 0.f;
+            Scur[c * kScanCols + j] = x;
+            dst[c * kD + cb + j] = x;
         }
     }
-    const int j = tid & (kD - 1), rows = tid >> 7;              // column j, rows 64 * rows ..
     for (int32_t k = s0 + 1; k < s1; ++k) {
         const int32_t prev = p.seg_info[k - 1].w;
         const float* A = seg_state(prev, 0);
         const float* B = seg_state(prev, 1);
         __syncthreads();                                         // Scur written, Am free
-        for (int e = tid; e < DD / 4; e += kScanThreads)
-            reinterpret_cast<float4*>(Am)[e] = reinterpret_cast<const float4*>(A)[e];
-        __syncthreads();
-        for (int r = 0; r < 64; ++r) {
-            const int c = 64 * rows + r;
-            const float4* arow = reinterpret_cast<const float4*>(Am + c * kD);
-            float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 8
-            for (int c4 = 0; c4 < kD / 4; ++c4) {
-                const float4 av = arow[c4];
-                acc0 = fmaf(av.x, Scur[(4 * c4) * kD + j], acc0);
-                acc1 = fmaf(av.y, Scur[(4 * c4 + 1) * kD + j], acc1);
-                acc0 = fmaf(av.z, Scur[(4 * c4 + 2) * kD + j], acc0);
-                acc1 = fmaf(av.w, Scur[(4 * c4 + 3) * kD + j], acc1);
-            }
-            Snew[c * kD + j] = (acc0 + acc1) + B[c * kD + j];
+        for (int e = tid; e < DD / 4; e += kScanThreads) {
+            const int r = e / (kD / 4), c4 = e % (kD / 4);
+            *reinterpret_cast<float4*>(Am + r * kLdA + 4 * c4) = reinterpret_cast<const float4*>(A)[e];
         }
         __syncthreads();
+        float acc[kD / 16];
+#pragma unroll
+        for (int m = 0; m < kD / 16; ++m) acc[m] = 0.f;
+        for (int u = 0; u < kD; u += 4) {
+            const float x0 = Scur[u * kScanCols + j], x1 = Scur[(u + 1) * kScanCols + j];
+            const float x2 = Scur[(u + 2) * kScanCols + j], x3 = Scur[(u + 3) * kScanCols + j];
+#pragma unroll
+            for (int m = 0; m < kD / 16; ++m) {
+                const float4 av = *reinterpret_cast<const float4*>(Am + (rg + 16 * m) * kLdA + u);
+                acc[m] = fmaf(av.x, x0, acc[m]);
+                acc[m] = fmaf(av.y, x1, acc[m]);
+                acc[m] = fmaf(av.z, x2, acc[m]);
+                acc[m] = fmaf(av.w, x3, acc[m]);
+            }
+        }
         // the segment's start state, and the snapshot at that boundary
         const int4 si = p.seg_info[k];
         float* dst = seg_state(si.w, 2);
@@ -507,14 +553,15 @@ __global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(ChunkLaunch 
                 if (slot >= 0 && (int64_t)slot < a.n_slots) snap = a.pool + (int64_t)slot * H * DD + head_off;
             }
         }
-        for (int e = tid; e < DD; e += kScanThreads) {
-            const float x = Snew[e];
-            dst[e] = x;
-            if (snap) snap[e] = x;
+        __syncthreads();                                         // every read of Scur done
+#pragma unroll
+        for (int m = 0; m < kD / 16; ++m) {
+            const int c = rg + 16 * m;
+            const float x = acc[m] + B[c * kD + cb + j];
+            Scur[c * kScanCols + j] = x;
+            dst[c * kD + cb + j] = x;
+            if (snap) snap[c * kD + cb + j] = x;
         }
-        float* t = Scur;
-        Scur = Snew;
-        Snew = t;
     }
 }
 
@@ -527,9 +574,9 @@ cudaError_t launch_segment_meta(const ChunkLaunch& p, cudaStream_t s) {
 }
 
 cudaError_t launch_segment_scan(const ChunkLaunch& p, cudaStream_t s) {
-    const int64_t blocks = (int64_t)p.a.n_seqs * p.a.n_heads;
+    const int64_t blocks = (int64_t)p.a.n_seqs * p.a.n_heads * kScanBlocks;
     if (blocks == 0) return cudaSuccess;
-    const size_t smem = 3 * (size_t)kD * kD * sizeof(float);
+    const size_t smem = ((size_t)kD * (kD + 4) + (size_t)kD * kScanCols) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(segment_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     note_launch();

@@ -113,6 +113,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking: has the phase with the given parity completed?  (test_wait
+// returns at once; try_wait may suspend the thread for a while before it
+// returns false, which an event loop polling several barriers cannot afford.)
+__device__ __forceinline__ bool mbar_done(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase with the given parity to complete; false after
 // `limit` clock cycles (about a second at the default) without completion.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
