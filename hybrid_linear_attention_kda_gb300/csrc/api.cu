@@ -145,7 +145,7 @@ int64_t max_segs_for(const kda_prefill_args* a) { return kda::max_segments(a->to
 int64_t max_scratch_for(const kda_prefill_args* a) { return kda::max_segments(a->total_tokens, a->n_seqs); }
 
 struct WorkspaceLayout {
-    size_t chunk_base, exact_count, exact_items, chunk_info, records, seg_info, seg_count, seg_state, total;
+    size_t chunk_base, exact_count, exact_items, chunk_info, records, seg_info, seg_count, seg_slow, seg_state, total;
     bool split;
 };
 
@@ -172,6 +172,8 @@ WorkspaceLayout layout_for(const kda_prefill_args* a) {
         off = round_up(off + sizeof(int4) * (size_t)max_segs_for(a), 256);
         w.seg_count = off;
         off = round_up(off + sizeof(int32_t) * ((size_t)a->n_seqs + 2), 256);
+        w.seg_slow = off;
+        off = round_up(off + sizeof(int32_t) * (size_t)max_scratch_for(a) * a->n_heads, 256);
         w.seg_state = off;
         off += (size_t)max_scratch_for(a) * a->n_heads * 3 * kda::kD * kda::kD * sizeof(float);
     }
@@ -277,6 +279,7 @@ kda_status_t prefill_impl(const kda_prefill_args* a, void* stream, Marks* m) {
     c.seg_info = w.split ? reinterpret_cast<int4*>(ws + w.seg_info) : nullptr;
     c.seg_count = w.split ? reinterpret_cast<int32_t*>(ws + w.seg_count) : nullptr;
     c.seg_state = w.split ? reinterpret_cast<float*>(ws + w.seg_state) : nullptr;
+    c.seg_slow = w.split ? reinterpret_cast<int32_t*>(ws + w.seg_slow) : nullptr;
     c.max_segs = w.split ? max_segs_for(a) : 0;
     KDA_MARK("chunk_meta");
     cudaError_t e = kda::launch_chunk_meta(c, s);
@@ -302,8 +305,14 @@ kda_status_t prefill_impl(const kda_prefill_args* a, void* stream, Marks* m) {
     e = kda::launch_chunk_exact(c, s);
     if (e != cudaSuccess) return cuda_fail(e, "prefill exact-item launch");
     if (w.split) {
-        // segment maps A (identity start, U~ = 0) and B (zero start), the scan of
+        // the tail windows before the segment boundaries (a head whose windows
+        // all forget their start state needs no segment map), the segment maps
+        // A (identity start, U~ = 0) and offsets B (zero start), the scan of
         // the segments' start states, then every segment in parallel
+        KDA_MARK("chunk_recur_tail");
+        c.mode = kda::kCarryTailMap;
+        e = kda::launch_chunk_recur(c, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill segment-tail launch");
         KDA_MARK("chunk_recur_map");
         c.mode = kda::kCarryMap;
         e = kda::launch_chunk_recur(c, s);

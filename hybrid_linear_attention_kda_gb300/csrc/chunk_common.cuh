@@ -69,7 +69,16 @@ enum CarryMode : int32_t {
     kCarryMap = 1,      // segments of split sequences: identity start, U~ = 0, writes A
     kCarryOffset = 2,   // segments of split sequences: zero start, writes B
     kCarryFinal = 3,    // every segment: outputs, snapshots, final state
+    kCarryTailMap = 4,  // the last kTailChunks chunks before each segment boundary: identity
+                        // start, U~ = 0; a boundary whose tail map is not exactly zero is
+                        // marked for the full map / offset / scan
 };
+
+// Chunks of the tail window before a segment boundary.  When the carry over the
+// window maps every state to exactly zero (the gates forgot it), the state at the
+// boundary is the window run from zero: the offset pass runs over the window
+// only and no segment map is needed.
+constexpr int64_t kTailChunks = 2;
 
 struct ChunkLaunch {
     kda_prefill_args a;
@@ -86,6 +95,8 @@ struct ChunkLaunch {
     int4* seg_info;        // [max_segs]: {sequence, first chunk within it, chunks, scratch index or -1}
     int32_t* seg_count;    // [1 + n_seqs + 1]: segments, then each sequence's first segment (and total)
     float* seg_state;      // [scratch, H, 3, kD, kD]: A, B, initial state of each split segment
+    int32_t* seg_slow;     // [scratch, H]: for the boundary at the start of a split segment
+                           // (not its sequence's first), nonzero = its tail map is not zero
     int64_t max_segs;
 };
 

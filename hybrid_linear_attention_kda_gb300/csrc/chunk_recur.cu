@@ -82,6 +82,24 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         ncs = si.z;
         scr = si.w;
         if (mode != kCarryFinal && scr < 0) return;   // only split sequences have segment maps
+        const bool first_seg = sidx == p.seg_count[1 + seq];
+        const bool final_seg = sidx + 1 == p.seg_count[2 + seq];
+        if (mode == kCarryTailMap) {
+            // the window before this segment's start (none before the first)
+            if (first_seg) return;
+            const int64_t w = coff < kTailChunks ? coff : kTailChunks;
+            coff -= w;
+            ncs = w;
+        } else if (mode == kCarryMap || mode == kCarryOffset) {
+            if (final_seg) return;                    // no boundary after the last segment
+            // the boundary at this segment's end (the next segment's start)
+            if (!p.seg_slow[(int64_t)p.seg_info[sidx + 1].w * H + h]) {
+                if (mode == kCarryMap) return;        // its tail map is zero: no map needed
+                const int64_t w = ncs < kTailChunks ? ncs : kTailChunks;
+                coff += ncs - w;                      // the offset over the tail window only
+                ncs = w;
+            }
+        }
     }
     int64_t tb, te, pos0;
     int32_t init;
@@ -94,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
     if (coff < 0 || coff + ncs > nc_seq) return;
     const bool last_seg = coff + ncs == nc_seq;
     const bool writes_out = mode == kCarryPlain || mode == kCarryFinal;
+    constexpr bool is_map = mode == kCarryMap || mode == kCarryTailMap;   // identity start, U~ = 0
     const int64_t g0 = g_seq + coff;
     const int64_t nc = ncs;
     tb += coff * kC;                // first packed token and absolute position of this chain
@@ -234,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
                 if (writes_out) {
                     if (!(ok = waitb(&ms.bar_c, par))) break;
                     w_c += 1;
-                } else if (mode == kCarryMap && ms.map_stop) {
+                } else if (is_map && ms.map_stop) {
                     stopped = true;                                 // the map is zero from here on
                     break;
                 }
@@ -271,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
             for (int i = 0; i < 64; ++i) S[i] = S0[(int64_t)(cbase + i) * kD + j];
         } else {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) S[i] = (mode == kCarryMap && cbase + i == j) ? 1.f : 0.f;
+            for (int i = 0; i < 64; ++i) S[i] = (is_map && cbase + i == j) ? 1.f : 0.f;
         }
         auto write_sa = [&]() {
 #pragma unroll
@@ -301,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
                 for (int e8 = 0; e8 < 2; ++e8) {
                     const int cc = 4 * ch + 2 * hf + e8;
                     // the segment map runs with U~ = 0
-                    const uint4 ut = mode == kCarryMap ? make_uint4(0u, 0u, 0u, 0u)
+                    const uint4 ut = is_map ? make_uint4(0u, 0u, 0u, 0u)
                                                        : *reinterpret_cast<const uint4*>(stage_p + kRecU + row64_chunk_off(j, cc));
                     const uint32_t uw[4] = {ut.x, ut.y, ut.z, ut.w};
                     uint32_t outw[4];
@@ -335,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
             // keeps it zero, so the map of the whole segment is zero and the pass
             // stops (an AND over the 256 state threads at named barrier 3)
             bool map_zero = false;
-            if (mode == kCarryMap) {
+            if (is_map) {
                 uint32_t z = 1;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) z &= S[i] == 0.f ? 1u : 0u;
@@ -375,8 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
         float* dst = nullptr;
         if (mode == kCarryMap || mode == kCarryOffset)
             dst = p.seg_state + ((int64_t)scr * H * 3 + (int64_t)h * 3 + (mode == kCarryMap ? 0 : 1)) * kD * kD;
-        else if (last_seg && a.final_state)
+        else if (writes_out && last_seg && a.final_state)
             dst = a.final_state + (int64_t)seq * slot_stride + head_off;
+        // the boundary's choice: a tail window that did not map every state to
+        // exactly zero takes the full map / offset / scan
+        if (mode == kCarryTailMap && tid == 0) p.seg_slow[(int64_t)scr * H + h] = (ok && ms.map_stop) ? 0 : 1;
         if (ok && dst) {
 #pragma unroll
             for (int i = 0; i < 64; ++i) dst[(int64_t)(cbase + i) * kD + j] = S[i];
@@ -520,25 +542,30 @@ __global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(ChunkLaunch 
         const int32_t prev = p.seg_info[k - 1].w;
         const float* A = seg_state(prev, 0);
         const float* B = seg_state(prev, 1);
-        __syncthreads();                                         // Scur written, Am free
-        for (int e = tid; e < DD / 4; e += kScanThreads) {
-            const int r = e / (kD / 4), c4 = e % (kD / 4);
-            *reinterpret_cast<float4*>(Am + r * kLdA + 4 * c4) = reinterpret_cast<const float4*>(A)[e];
-        }
-        __syncthreads();
+        // a boundary whose tail map is zero starts the segment from the tail-window
+        // offset B alone
+        const bool slow = p.seg_slow[(int64_t)p.seg_info[k].w * H + h] != 0;
         float acc[kD / 16];
 #pragma unroll
         for (int m = 0; m < kD / 16; ++m) acc[m] = 0.f;
-        for (int u = 0; u < kD; u += 4) {
-            const float x0 = Scur[u * kScanCols + j], x1 = Scur[(u + 1) * kScanCols + j];
-            const float x2 = Scur[(u + 2) * kScanCols + j], x3 = Scur[(u + 3) * kScanCols + j];
+        if (slow) {
+            __syncthreads();                                     // Scur written, Am free
+            for (int e = tid; e < DD / 4; e += kScanThreads) {
+                const int r = e / (kD / 4), c4 = e % (kD / 4);
+                *reinterpret_cast<float4*>(Am + r * kLdA + 4 * c4) = reinterpret_cast<const float4*>(A)[e];
+            }
+            __syncthreads();
+            for (int u = 0; u < kD; u += 4) {
+                const float x0 = Scur[u * kScanCols + j], x1 = Scur[(u + 1) * kScanCols + j];
+                const float x2 = Scur[(u + 2) * kScanCols + j], x3 = Scur[(u + 3) * kScanCols + j];
 #pragma unroll
-            for (int m = 0; m < kD / 16; ++m) {
-                const float4 av = *reinterpret_cast<const float4*>(Am + (rg + 16 * m) * kLdA + u);
-                acc[m] = fmaf(av.x, x0, acc[m]);
-                acc[m] = fmaf(av.y, x1, acc[m]);
-                acc[m] = fmaf(av.z, x2, acc[m]);
-                acc[m] = fmaf(av.w, x3, acc[m]);
+                for (int m = 0; m < kD / 16; ++m) {
+                    const float4 av = *reinterpret_cast<const float4*>(Am + (rg + 16 * m) * kLdA + u);
+                    acc[m] = fmaf(av.x, x0, acc[m]);
+                    acc[m] = fmaf(av.y, x1, acc[m]);
+                    acc[m] = fmaf(av.z, x2, acc[m]);
+                    acc[m] = fmaf(av.w, x3, acc[m]);
+                }
             }
         }
         // the segment's start state, and the snapshot at that boundary
@@ -601,6 +628,7 @@ cudaError_t launch_chunk_recur(const ChunkLaunch& p, cudaStream_t s) {
         case kCarryMap: return launch_recur_mode<kCarryMap>(p, s);
         case kCarryOffset: return launch_recur_mode<kCarryOffset>(p, s);
         case kCarryFinal: return launch_recur_mode<kCarryFinal>(p, s);
+        case kCarryTailMap: return launch_recur_mode<kCarryTailMap>(p, s);
         default: return launch_recur_mode<kCarryPlain>(p, s);
     }
 }
