@@ -84,36 +84,18 @@ struct LocalMaps {
     CUtensorMap q, k, v, alpha;   // 2-D views [T_tot rows x H*128 elements]
 };
 
-__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
 __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
     return make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
                       pack_bf16(v[6], v[7]));
 }
 __device__ __forceinline__ void sts16(uint32_t saddr, uint4 v) { st_shared_v4(saddr, v.x, v.y, v.z, v.w); }
 __device__ __forceinline__ void stg16(uint8_t* gaddr, uint4 v) { *reinterpret_cast<uint4*>(gaddr) = v; }
-
-// Eight bf16 values gathered one at a time (index e = 0..7, ascending) and kept
-// as packed pairs: a float waits only for its partner.
-struct Pack8 {
-    uint32_t w[4];
-    float pend;
-    __device__ __forceinline__ void put(int e, float x) {
-        if (e & 1) w[e >> 1] = pack_bf16(pend, x);
-        else pend = x;
-    }
-    __device__ __forceinline__ uint4 get() const { return make_uint4(w[0], w[1], w[2], w[3]); }
-};
-// The same for a walk in decreasing order (the odd element arrives first).
-struct Pack8Rev {
-    uint32_t w[4];
-    float pend;
-    __device__ __forceinline__ void put(int e, float x) {
-        if (e & 1) pend = x;
-        else w[e >> 1] = pack_bf16(x, pend);
-    }
-    __device__ __forceinline__ uint4 get() const { return make_uint4(w[0], w[1], w[2], w[3]); }
-};
+// two bf16 (low half the even token) times two bf16 factors, rounded once
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t x, uint32_t f) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(f));
+    return r;
+}
 
 // byte offset of the 16-byte chunk (mn .. mn+7, k) of an MN-major tile
 __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
@@ -376,78 +358,85 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             const float xi_rest = qq == 0 ? Q1 * Q2 : Q2;      // tokens after the quarter, up to 47
             if (qq == 0) reinterpret_cast<float*>(rec + kRecG)[c] = (Q0 * Q1) * (Q2 * Q3);
             const uint32_t apa = Rs + kRa, apb = Rs + kRb;
+            // Each factor is formed in fp32 and rounded to bf16 once; a pair of
+            // tokens (2j, 2j+1) of one channel is scaled by one packed multiply.
             {   // forward: Gamma -> Q~ (record), X^T = Gamma k
-                float P = 1.f;
-                Pack8 gq, xk;
+                float G = before;
+                uint32_t gq[4], xk[4];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
-                    const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-                    P *= al[i];
-                    const float G = before * P;
-                    gq.put(i & 7, qf * G);
-                    xk.put(i & 7, kf * G);
-                    if ((i & 7) == 7) {
+                for (int i = 0; i < 16; i += 2) {
+                    const float G0 = G * al[i];
+                    G = G0 * al[i + 1];
+                    const uint32_t f = pack_bf16(G0, G);
+                    gq[(i & 7) >> 1] = mul_bf16x2(qp[i >> 1], f);
+                    xk[(i & 7) >> 1] = mul_bf16x2(kp[i >> 1], f);
+                    if ((i & 7) == 6) {
                         const uint32_t r0 = r_base + (i & ~7);
-                        stg16(rec + kRecQ + row64_chunk_off(c, r0 >> 3), gq.get());
-                        sts16(s_base + kX + row64_chunk_off(c, r0 >> 3), xk.get());
+                        stg16(rec + kRecQ + row64_chunk_off(c, r0 >> 3), make_uint4(gq[0], gq[1], gq[2], gq[3]));
+                        sts16(s_base + kX + row64_chunk_off(c, r0 >> 3), make_uint4(xk[0], xk[1], xk[2], xk[3]));
                     }
                 }
             }
             if (sub) {   // up from the half's reference token: phi = E, psi = 1/E
                 float E = 1.f;
-                Pack8 dq, dk, dd;
+                uint32_t dq[4], dk[4], dd[4];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
-                    const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-                    E *= al[i];
-                    guard_bad |= !(E >= kGuardMin);
-                    const float inv = __fdividef(1.f, E);
-                    dq.put(i & 7, qf * E);
-                    dk.put(i & 7, kf * E);
-                    dd.put(i & 7, kf * inv);
-                    if ((i & 7) == 7) {
+                for (int i = 0; i < 16; i += 2) {
+                    const float E0 = E * al[i];
+                    E = E0 * al[i + 1];
+                    guard_bad |= !(E >= kGuardMin);      // alphas lie in [0, 1]: E <= E0
+                    const uint32_t fe = pack_bf16(E0, E);
+                    const uint32_t fi = pack_bf16(__fdividef(1.f, E0), __fdividef(1.f, E));
+                    dq[(i & 7) >> 1] = mul_bf16x2(qp[i >> 1], fe);
+                    dk[(i & 7) >> 1] = mul_bf16x2(kp[i >> 1], fe);
+                    dd[(i & 7) >> 1] = mul_bf16x2(kp[i >> 1], fi);
+                    if ((i & 7) == 6) {
                         const uint32_t r0 = r_base + (i & ~7);
-                        sts16(apb + mn_chunk(r0, cl), dq.get());
-                        sts16(apb + mn_chunk(64 + r0, cl), dk.get());
-                        sts16(apa + mn_chunk(r0, cl), dd.get());
+                        sts16(apb + mn_chunk(r0, cl), make_uint4(dq[0], dq[1], dq[2], dq[3]));
+                        sts16(apb + mn_chunk(64 + r0, cl), make_uint4(dk[0], dk[1], dk[2], dk[3]));
+                        sts16(apa + mn_chunk(r0, cl), make_uint4(dd[0], dd[1], dd[2], dd[3]));
                     }
                 }
             }
             {   // backward: kappa -> Kbar (record); half 0 also xi
-                float Q = 1.f;
-                Pack8Rev kb, kx;
+                float Qa = after, Qx = xi_rest;     // the suffix product times the factor beyond the quarter
+                uint32_t kb[4], kx[4];
 #pragma unroll
-                for (int i = 15; i >= 0; --i) {
-                    const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-                    kb.put(i & 7, kf * (Q * after));
-                    if (!hh) kx.put(i & 7, kf * (Q * xi_rest));
+                for (int i = 14; i >= 0; i -= 2) {
+                    const float a1 = Qa, x1 = Qx;   // token i + 1
+                    Qa *= al[i + 1];
+                    kb[(i & 7) >> 1] = mul_bf16x2(kp[i >> 1], pack_bf16(Qa, a1));
+                    if (!hh) {
+                        Qx *= al[i + 1];
+                        kx[(i & 7) >> 1] = mul_bf16x2(kp[i >> 1], pack_bf16(Qx, x1));
+                        Qx *= al[i];
+                    }
+                    Qa *= al[i];
                     if ((i & 7) == 0) {
                         const uint32_t r0 = r_base + i;
-                        stg16(rec + kRecK + row64_chunk_off(c, r0 >> 3), kb.get());
-                        if (!hh) sts16(apa + mn_chunk(64 + r0, cl), kx.get());
+                        stg16(rec + kRecK + row64_chunk_off(c, r0 >> 3), make_uint4(kb[0], kb[1], kb[2], kb[3]));
+                        if (!hh) sts16(apa + mn_chunk(64 + r0, cl), make_uint4(kx[0], kx[1], kx[2], kx[3]));
                     }
-                    Q *= al[i];
                 }
             }
             if (!sub) {  // down to the half's reference token: phi = 1/D, psi = D
                 float D = 1.f;
-                Pack8Rev dq, dk, dd;
+                uint32_t dq[4], dk[4], dd[4];
 #pragma unroll
-                for (int i = 15; i >= 0; --i) {
-                    const float qf = (i & 1) ? bf_hi(qp[i >> 1]) : bf_lo(qp[i >> 1]);
-                    const float kf = (i & 1) ? bf_hi(kp[i >> 1]) : bf_lo(kp[i >> 1]);
-                    guard_bad |= !(D >= kGuardMin);
-                    const float inv = __fdividef(1.f, D);
-                    dq.put(i & 7, qf * inv);
-                    dk.put(i & 7, kf * inv);
-                    dd.put(i & 7, kf * D);
+                for (int i = 14; i >= 0; i -= 2) {
+                    const float D1 = D;             // token i + 1
+                    D *= al[i + 1];                 // token i
+                    guard_bad |= !(D >= kGuardMin); // alphas lie in [0, 1]: D <= D1
+                    const uint32_t fi = pack_bf16(__fdividef(1.f, D), __fdividef(1.f, D1));
+                    const uint32_t fd = pack_bf16(D, D1);
+                    dq[(i & 7) >> 1] = mul_bf16x2(qp[i >> 1], fi);
+                    dk[(i & 7) >> 1] = mul_bf16x2(kp[i >> 1], fi);
+                    dd[(i & 7) >> 1] = mul_bf16x2(kp[i >> 1], fd);
                     if ((i & 7) == 0) {
                         const uint32_t r0 = r_base + i;
-                        sts16(apb + mn_chunk(r0, cl), dq.get());
-                        sts16(apb + mn_chunk(64 + r0, cl), dk.get());
-                        sts16(apa + mn_chunk(r0, cl), dd.get());
+                        sts16(apb + mn_chunk(r0, cl), make_uint4(dq[0], dq[1], dq[2], dq[3]));
+                        sts16(apb + mn_chunk(64 + r0, cl), make_uint4(dk[0], dk[1], dk[2], dk[3]));
+                        sts16(apa + mn_chunk(r0, cl), make_uint4(dd[0], dd[1], dd[2], dd[3]));
                     }
                     D *= al[i];
                 }
