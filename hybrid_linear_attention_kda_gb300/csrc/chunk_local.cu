@@ -201,6 +201,20 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
     }
 }
 
+// Tokens n .. 63 of both rounds' staged tiles become alpha = 1, q = k = 0 (a
+// partial chunk; kept out of line, off the path of whole chunks).
+__device__ __noinline__ void mask_tail_tokens(uint8_t* sm, int n, int tid) {
+    const int rows = kC - n;
+    for (int idx = tid; idx < 2 * rows * 64; idx += kThreads) {
+        const int g = idx / (rows * 64), rem = idx - g * rows * 64;
+        const int e = (n + (rem >> 6)) * 64 + (rem & 63);
+        uint8_t* R = sm + g * kRound;
+        reinterpret_cast<float*>(R + kRal)[e] = 1.f;
+        reinterpret_cast<uint16_t*>(R + kRq)[e] = 0;
+        reinterpret_cast<uint16_t*>(R + kRk)[e] = 0;
+    }
+}
+
 struct Item {
     int64_t g;     // global chunk
     int h;         // head
@@ -319,6 +333,13 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             break;
         }
 
+        if (n < kC) {
+            // a partial chunk: its missing tokens become alpha = 1, q = k = 0 in
+            // the staged tiles, so the gate products need no token masks
+            mask_tail_tokens(sm, n, tid);
+            __syncthreads();
+        }
+
         // ------------------------------------------------------------ phase 1: gates, operands
         // Decay factors of channel c for the quarter's tokens, with m the 16th
         // token of the half: Gamma (chunk prefix), kappa (chunk suffix),
@@ -340,11 +361,10 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < 16; i += 2) {
                 const int r = r_base + i;
-                const bool v0 = r < n, v1 = r + 1 < n;
-                al[i] = v0 ? sal[r * 64 + cl] : 1.f;
-                al[i + 1] = v1 ? sal[(r + 1) * 64 + cl] : 1.f;
-                qp[i >> 1] = (v0 ? (uint32_t)sq[r * 64 + cl] : 0u) | ((v1 ? (uint32_t)sq[(r + 1) * 64 + cl] : 0u) << 16);
-                kp[i >> 1] = (v0 ? (uint32_t)sk[r * 64 + cl] : 0u) | ((v1 ? (uint32_t)sk[(r + 1) * 64 + cl] : 0u) << 16);
+                al[i] = sal[r * 64 + cl];
+                al[i + 1] = sal[(r + 1) * 64 + cl];
+                qp[i >> 1] = (uint32_t)sq[r * 64 + cl] | ((uint32_t)sq[(r + 1) * 64 + cl] << 16);
+                kp[i >> 1] = (uint32_t)sk[r * 64 + cl] | ((uint32_t)sk[(r + 1) * 64 + cl] << 16);
                 own *= al[i];
                 own *= al[i + 1];
             }
@@ -539,11 +559,11 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
                           reinterpret_cast<float*>(sm + kTscr), tid);
         {   // T'^T row s = beta_s (column s of T, zero above the diagonal), the MN-major [s][r] operand
             const float* Tf = reinterpret_cast<const float*>(sm + kTf);
-            const int srow = tid >> 2;
+            const int srow = tid & 63;            // a warp reads 32 consecutive columns of T
             const float bs = bsm[srow];
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
-                const int cc = 2 * (tid & 3) + q2;
+                const int cc = 2 * (tid >> 6) + q2;
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
