@@ -496,47 +496,58 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         fence_after_sync();
 
         // ------------------------------------------------------------ phase 2: P to the record, A to smem
+        // warps 3 and 7 hold no TMEM lanes with data: they write the zero blocks
         if (warp < 3) {
             const int s = warp == 2 ? lane : lane + 32 * warp;      // key token of this TMEM lane
             const int col0 = warp == 0 ? 0 : 32;
+            uint32_t v[2][16];
+            tmem_ld16(tbase + lanebase + col0, v[0]);
+            tmem_ld16(tbase + lanebase + col0 + 16, v[1]);
+            tmem_wait_ld();
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                uint32_t v[16];
-                tmem_ld16(tbase + lanebase + col0 + 16 * hf, v);
-                tmem_wait_ld();
 #pragma unroll
                 for (int e8 = 0; e8 < 2; ++e8) {
                     const int r0 = col0 + 16 * hf + 8 * e8;
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        x[e] = (warp == 2 || r0 + e >= s) ? __uint_as_float(v[8 * e8 + e]) : 0.f;
+                        x[e] = (warp == 2 || r0 + e >= s) ? __uint_as_float(v[hf][8 * e8 + e]) : 0.f;
                     sts16(s_base + kPst + row64_chunk_off(s, r0 >> 3), pack8(x));
                 }
             }
-            if (warp == 1) {
+        } else if (warp == 3) {          // P rows 32..63, columns 0..31 (keys after the query)
+            const int s = lane + 32;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) sts16(s_base + kPst + row64_chunk_off(s, cc), make_uint4(0u, 0u, 0u, 0u));
-            }
-        } else if (warp >= 4 && warp < 7) {
+            for (int cc = 0; cc < 4; ++cc) sts16(s_base + kPst + row64_chunk_off(s, cc), make_uint4(0u, 0u, 0u, 0u));
+        } else if (warp < 7) {
             const int wq = warp - 4;
             const int s = wq == 2 ? lane : lane + 32 * wq;
             const int col0 = wq == 0 ? 64 : 96;                     // columns 64 + r
             float* Am = reinterpret_cast<float*>(sm + kAmat);
+            uint32_t v[2][16];
+            tmem_ld16(tbase + lanebase + col0, v[0]);
+            tmem_ld16(tbase + lanebase + col0 + 16, v[1]);
+            tmem_wait_ld();
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                uint32_t v[16];
-                tmem_ld16(tbase + lanebase + col0 + 16 * hf, v);
-                tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int r = col0 - 64 + 16 * hf + e;
-                    Am[r * kC + s] = (wq == 2 || r > s) ? bsm[r] * __uint_as_float(v[e]) : 0.f;
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const int r4 = col0 - 64 + 16 * hf + 4 * e4;
+                    const float4 b4 = *reinterpret_cast<const float4*>(bsm + r4);
+                    const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = r4 + e;
+                        Am[r * kC + s] = (wq == 2 || r > s) ? bb[e] * __uint_as_float(v[hf][4 * e4 + e]) : 0.f;
+                    }
                 }
             }
-            if (wq == 1) {
-                for (int r = 0; r < 32; ++r) Am[r * kC + s] = 0.f;
-            }
+        } else {                          // A rows 0..31, columns 32..63 (above the diagonal)
+            float* Am = reinterpret_cast<float*>(sm + kAmat);
+            const int s = lane + 32;
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r) Am[r * kC + s] = 0.f;
         }
         fence_async_smem();
         fence_before_sync();
@@ -616,16 +627,17 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             const uint32_t col0 = warp < 4 ? 0u : 64u;
             const uint32_t dst = s_base + kWst + (warp < 4 ? 0u : 16384u);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t v[16];
-                tmem_ld16(tbase + lanebase + col0 + 16 * q4, v);
+            for (int q2 = 0; q2 < 2; ++q2) {
+                uint32_t v[2][16];
+                tmem_ld16(tbase + lanebase + col0 + 32 * q2, v[0]);
+                tmem_ld16(tbase + lanebase + col0 + 32 * q2 + 16, v[1]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e8 = 0; e8 < 2; ++e8) {
+                for (int e8 = 0; e8 < 4; ++e8) {
                     float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * e8 + e]);
-                    sts16(dst + row64_chunk_off(row, 2 * q4 + e8), pack8(x));
+                    for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[e8 >> 1][8 * (e8 & 1) + e]);
+                    sts16(dst + row64_chunk_off(row, 4 * q2 + e8), pack8(x));
                 }
             }
         }
