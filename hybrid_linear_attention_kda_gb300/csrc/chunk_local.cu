@@ -109,7 +109,9 @@ __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
 //     T_ij = -T_ii (A_ij T_jj)       (for the block partition at that level).
 // All 256 threads take part; T (zeros above the diagonal inside the diagonal
 // blocks) goes to Tf, row-major.  scr holds 1024 floats.  Ends with a barrier.
-__device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, float* scr, int tid) {
+template <class Side, class AfterStage1>
+__device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, float* scr, int tid, Side side,
+                                                  AfterStage1 after_stage1) {
     if (tid < kC) {
         const int o = 16 * (tid >> 4), jj = tid & 15;
         float t[16];
@@ -122,16 +124,19 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tf[(o + r) * kC + o + jj] = t[r];
-    } else if (tid < 3 * kC) {
+    } else if (tid < 2 * kC) {
         // blocks (0,1) and (2,3) are zero; the 32 x 32 level reads them
-        const int e = tid - kC, b = e >> 6, x = e & 63;       // 2 blocks x 256 entries, 4 per thread
+        const int e = tid - kC, b = e >> 5, x = e & 31;       // 2 blocks x 256 entries, 8 per thread
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int idx = x + 64 * m, rr = idx >> 4, cc = idx & 15;
+        for (int m = 0; m < 8; ++m) {
+            const int idx = x + 32 * m, rr = idx >> 4, cc = idx & 15;
             Tf[(32 * b + rr) * kC + 32 * b + 16 + cc] = 0.f;
         }
+    } else {
+        side();       // warps 4-7: work of the caller's that does not depend on T
     }
     __syncthreads();
+    if (tid == 0) after_stage1();
     {   // blocks (1,0) and (3,2): M = A_ij T_jj, then T_ij = -T_ii M
         const int rr = tid >> 4, cc = tid & 15;
 #pragma unroll
@@ -496,67 +501,37 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         fence_after_sync();
 
         // ------------------------------------------------------------ phase 2: P to the record, A to smem
-        // warps 3 and 7 hold no TMEM lanes with data: they write the zero blocks
-        if (warp < 3) {
-            const int s = warp == 2 ? lane : lane + 32 * warp;      // key token of this TMEM lane
-            const int col0 = warp == 0 ? 0 : 32;
-            uint32_t v[2][16];
-            tmem_ld16(tbase + lanebase + col0, v[0]);
-            tmem_ld16(tbase + lanebase + col0 + 16, v[1]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-                for (int e8 = 0; e8 < 2; ++e8) {
-                    const int r0 = col0 + 16 * hf + 8 * e8;
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        x[e] = (warp == 2 || r0 + e >= s) ? __uint_as_float(v[hf][8 * e8 + e]) : 0.f;
-                    sts16(s_base + kPst + row64_chunk_off(s, r0 >> 3), pack8(x));
-                }
-            }
-        } else if (warp == 3) {          // P rows 32..63, columns 0..31 (keys after the query)
-            const int s = lane + 32;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) sts16(s_base + kPst + row64_chunk_off(s, cc), make_uint4(0u, 0u, 0u, 0u));
-        } else if (warp < 7) {
-            const int wq = warp - 4;
-            const int s = wq == 2 ? lane : lane + 32 * wq;
-            const int col0 = wq == 0 ? 64 : 96;                     // columns 64 + r
+        // A to shared memory: warps w and w + 4 share TMEM lane quarter w (16 columns
+        // each); warps 3 and 7 hold no lanes with data and write A's zero block
+        {
             float* Am = reinterpret_cast<float*>(sm + kAmat);
-            uint32_t v[2][16];
-            tmem_ld16(tbase + lanebase + col0, v[0]);
-            tmem_ld16(tbase + lanebase + col0 + 16, v[1]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+            const int wq = warp & 3, hf = warp >> 2;
+            if (wq < 3) {
+                const int s = wq == 2 ? lane : lane + 32 * wq;
+                const int col0 = (wq == 0 ? 64 : 96) + 16 * hf;     // columns 64 + r
+                uint32_t v[16];
+                tmem_ld16(tbase + lanebase + col0, v);
+                tmem_wait_ld();
 #pragma unroll
                 for (int e4 = 0; e4 < 4; ++e4) {
-                    const int r4 = col0 - 64 + 16 * hf + 4 * e4;
+                    const int r4 = col0 - 64 + 4 * e4;
                     const float4 b4 = *reinterpret_cast<const float4*>(bsm + r4);
                     const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int r = r4 + e;
-                        Am[r * kC + s] = (wq == 2 || r > s) ? bb[e] * __uint_as_float(v[hf][4 * e4 + e]) : 0.f;
+                        Am[r * kC + s] = (wq == 2 || r > s) ? bb[e] * __uint_as_float(v[4 * e4 + e]) : 0.f;
                     }
                 }
-            }
-        } else {                          // A rows 0..31, columns 32..63 (above the diagonal)
-            float* Am = reinterpret_cast<float*>(sm + kAmat);
-            const int s = lane + 32;
+            } else {                      // rows 16 hf .. 16 hf + 15, columns 32..63 (above the diagonal)
+                const int s = lane + 32;
 #pragma unroll 8
-            for (int r = 0; r < 32; ++r) Am[r * kC + s] = 0.f;
+                for (int r = 16 * hf; r < 16 * hf + 16; ++r) Am[r * kC + s] = 0.f;
+            }
         }
-        fence_async_smem();
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
-        if (tid == 0) {
-            bulk_s2g(rec + kRecP, sm + kPst, 8192);
-            bulk_commit();
-        }
 
         // the next item's beta: loaded now, stored after phase 4, so the global
         // load's latency passes while T is inverted
@@ -566,8 +541,42 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             if (tid < nx.n) beta_nx = a.beta[(nx.t0 + tid) * H + nx.h];
         }
         // ------------------------------------------------------------ phase 3: T
+        // P leaves TMEM while the diagonal blocks of T are solved: warps 4-6 hold
+        // TMEM lane quarters 0-2, warp 7 writes P's zero block
+        auto p_to_staging = [&]() {
+            const int wq = warp & 3;
+            if (wq < 3) {
+                const int s = wq == 2 ? lane : lane + 32 * wq;      // key token of this TMEM lane
+                const int col0 = wq == 0 ? 0 : 32;
+                uint32_t v[2][16];
+                tmem_ld16(tbase + lanebase + col0, v[0]);
+                tmem_ld16(tbase + lanebase + col0 + 16, v[1]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                    for (int e8 = 0; e8 < 2; ++e8) {
+                        const int r0 = col0 + 16 * hf + 8 * e8;
+                        float x[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            x[e] = (wq == 2 || r0 + e >= s) ? __uint_as_float(v[hf][8 * e8 + e]) : 0.f;
+                        sts16(s_base + kPst + row64_chunk_off(s, r0 >> 3), pack8(x));
+                    }
+                }
+            } else {                      // rows 32..63, columns 0..31 (keys after the query)
+                const int s = lane + 32;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) sts16(s_base + kPst + row64_chunk_off(s, cc), make_uint4(0u, 0u, 0u, 0u));
+            }
+            fence_async_smem();
+        };
+        auto store_p = [&]() {
+            bulk_s2g(rec + kRecP, sm + kPst, 8192);
+            bulk_commit();
+        };
         invert_unit_lower(reinterpret_cast<const float*>(sm + kAmat), reinterpret_cast<float*>(sm + kTf),
-                          reinterpret_cast<float*>(sm + kTscr), tid);
+                          reinterpret_cast<float*>(sm + kTscr), tid, p_to_staging, store_p);
         {   // T'^T row s = beta_s (column s of T, zero above the diagonal), the MN-major [s][r] operand
             const float* Tf = reinterpret_cast<const float*>(sm + kTf);
             const int srow = tid & 63;            // a warp reads 32 consecutive columns of T
