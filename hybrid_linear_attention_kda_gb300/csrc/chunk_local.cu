@@ -53,7 +53,8 @@ constexpr uint32_t kRa = 0, kRb = 16384;   // APa / APb K-slices: MN-major [8-ch
 constexpr uint32_t kSv = 65536;            // v: two 128-byte-swizzled [64 t][64 c] boxes, 8 KiB apart
 constexpr uint32_t kVbox = 8192;
 constexpr uint32_t kX = 81920;             // X^T = (Gamma k)^T, K-major [c][t]
-constexpr uint32_t kLoadBytes = 81920;     // q, k, v and alpha of one item
+constexpr uint32_t kLoadBytes = 65536;     // q, k and alpha of one item
+constexpr uint32_t kVBytes = 16384;        // its v
 constexpr uint32_t kLbo = 1024, kSbo = 2048;
 // [0, 64 KiB) once the A/P MMA has read its operands:
 constexpr uint32_t kAmat = 0;              // A fp32 [64][64]
@@ -70,12 +71,13 @@ struct Misc {
     float beta[2][kC];         // this item's and the next item's beta
     int4 info[2];              // this item's and the next item's chunk-table entry
     float qprod[2][4][64];     // per round: product of alpha over each 16-token quarter, per channel
-    uint64_t bar_load;
+    uint64_t bar_load;         // q, k and alpha
+    uint64_t bar_v;            // v, waited for only by the W / U~ product
     uint64_t bar_mma;
     uint32_t tslot;
     int32_t guard_fail;
     // copies and MMAs thread 0 issued and waited for, to drain on a timeout
-    uint32_t ld_issued, ld_waited, mma_issued, mma_waited;
+    uint32_t ld_issued, ld_waited, v_issued, v_waited, mma_issued, mma_waited;
 };
 constexpr size_t kSmemBytes = kMisc + sizeof(Misc) + 1024;
 static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
@@ -262,14 +264,15 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
     if (warp == 0) tmem_alloc(&ms.tslot, kTmemCols);
     if (tid == 0) {
         mbar_init(&ms.bar_load, 1);
+        mbar_init(&ms.bar_v, 1);
         mbar_init(&ms.bar_mma, 1);
         ms.guard_fail = 0;
-        ms.ld_issued = ms.ld_waited = ms.mma_issued = ms.mma_waited = 0;
+        ms.ld_issued = ms.ld_waited = ms.v_issued = ms.v_waited = ms.mma_issued = ms.mma_waited = 0;
         fence_mbar_init();
     }
-    // thread 0 issues every copy and MMA and counts them, to drain on a timeout
-    // an item's q, k and alpha (with the whole 80 KiB expected on the barrier),
-    // then, once the staging above them has been read, its v
+    // thread 0 issues every copy and MMA and counts them, to drain on a timeout:
+    // an item's q, k and alpha, then, once the staging above them has been read,
+    // its v on a barrier of its own (the gate products start without it)
     auto issue_load_qka = [&](int64_t item, int4 info) {
         const Item it = decode_item(p, item, info);
         mbar_expect_tx(&ms.bar_load, kLoadBytes);
@@ -287,7 +290,10 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         const Item it = decode_item(p, item, info);
         const int32_t x = it.h * kD, y = (int32_t)it.t0;
 #pragma unroll
-        for (int g = 0; g < 2; ++g) tma_load_2d(sm + kSv + g * kVbox, &tm.v, x + 64 * g, y, &ms.bar_load);
+        mbar_expect_tx(&ms.bar_v, kVBytes);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) tma_load_2d(sm + kSv + g * kVbox, &tm.v, x + 64 * g, y, &ms.bar_v);
+        ms.v_issued += 1;
     };
     fence_before_sync();
     __syncthreads();
@@ -599,6 +605,10 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         fence_after_sync();
 
         if (tid == 0) {
+            ok = mbar_wait(&ms.bar_v, (uint32_t)(k & 1));
+            if (ok) ms.v_waited += 1;
+        }
+        if (tid == 0 && ok) {
             // W^T = X^T T'^T (X^T K-major); U~^T = V^T T'^T with V^T the swizzled
             // v tile read MN-major (64-channel blocks 8 KiB apart, 8-token groups 1 KiB apart)
             const uint32_t idesc_k = idesc_bf16(128, 64, false, true);
@@ -614,7 +624,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             mma_commit(&ms.bar_mma);
             ms.mma_issued += 1;
         }
-        if (tid == 0) {
+        if (tid == 0 && ok) {
             ok = mbar_wait(&ms.bar_mma, 1);
             if (ok) ms.mma_waited += 1;
         }
@@ -673,6 +683,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         // shared and tensor memory are released
         flag(p.status, KDA_DEV_WAIT_TIMEOUT);
         for (uint32_t l = ms.ld_waited; l < ms.ld_issued; ++l) mbar_wait(&ms.bar_load, l & 1);
+        for (uint32_t l = ms.v_waited; l < ms.v_issued; ++l) mbar_wait(&ms.bar_v, l & 1);
         for (uint32_t m = ms.mma_waited; m < ms.mma_issued; ++m) mbar_wait(&ms.bar_mma, m & 1);
     }
     fence_before_sync();
