@@ -289,7 +289,6 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
     auto issue_load_v = [&](int64_t item, int4 info) {
         const Item it = decode_item(p, item, info);
         const int32_t x = it.h * kD, y = (int32_t)it.t0;
-#pragma unroll
         mbar_expect_tx(&ms.bar_v, kVBytes);
 #pragma unroll
         for (int g = 0; g < 2; ++g) tma_load_2d(sm + kSv + g * kVbox, &tm.v, x + 64 * g, y, &ms.bar_v);
