@@ -248,6 +248,7 @@ __device__ __forceinline__ Item decode_item(const ChunkLaunch& p, int64_t item, 
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant__ LocalMaps tm) {
+    griddep_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Misc& ms = *reinterpret_cast<Misc*>(sm + kMisc);
@@ -712,6 +713,7 @@ __device__ __forceinline__ void st_bf16(uint8_t* p, float x) {
 }
 
 __global__ void __launch_bounds__(kExactThreads) chunk_exact_kernel(ChunkLaunch p) {
+    griddep_wait();
     extern __shared__ __align__(16) uint8_t exact_smem[];
     ExactSmem& sm = *reinterpret_cast<ExactSmem*>(exact_smem);
     const kda_prefill_args& a = p.a;
@@ -807,6 +809,7 @@ __global__ void __launch_bounds__(kExactThreads) chunk_exact_kernel(ChunkLaunch 
 // chunk_base[s] = first global chunk of sequence s (exclusive scan of
 // ceil(L_s / 64) over valid sequences).
 __global__ void __launch_bounds__(1024) chunk_meta_kernel(ChunkLaunch p) {
+    griddep_wait();
     const kda_prefill_args& a = p.a;
     const int n = a.n_seqs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -891,14 +894,12 @@ cudaError_t launch_chunk_exact(const ChunkLaunch& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int64_t grid = max_items < 2 * (int64_t)sms ? max_items : 2 * (int64_t)sms;
     note_launch();
-    chunk_exact_kernel<<<(unsigned)grid, kExactThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(chunk_exact_kernel, dim3((unsigned)grid), dim3(kExactThreads), smem, s, p);
 }
 
 cudaError_t launch_chunk_meta(const ChunkLaunch& p, cudaStream_t s) {
     note_launch();
-    chunk_meta_kernel<<<1, 1024, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(chunk_meta_kernel, dim3(1), dim3(1024), 0, s, p);
 }
 
 namespace {
@@ -964,8 +965,7 @@ cudaError_t launch_chunk_local(const ChunkLaunch& p, cudaStream_t s) {
     const int64_t slots = (int64_t)kCtasPerSm * sms;
     const int64_t grid = max_items < slots ? max_items : slots;
     note_launch();
-    chunk_local_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(p, tm);
-    return cudaGetLastError();
+    return launch_overlapped(chunk_local_kernel, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, p, tm);
 }
 
 }  // namespace kda

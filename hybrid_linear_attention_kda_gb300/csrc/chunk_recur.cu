@@ -58,6 +58,7 @@ __device__ __forceinline__ void sts16(uint32_t saddr, uint4 v) { st_shared_v4(sa
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p) {
+    griddep_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Misc& ms = *reinterpret_cast<Misc*>(sm + kMisc);
@@ -465,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_recur_kernel(ChunkLaunch p)
 // sequences at most take this path (fewer chains than half the SMs), so one
 // thread builds the table.
 __global__ void segment_meta_kernel(ChunkLaunch p) {
+    griddep_wait();
     if (threadIdx.x != 0) return;
     const kda_prefill_args& a = p.a;
     const int64_t max_scr = max_segments(a.total_tokens, a.n_seqs);
@@ -507,6 +509,7 @@ constexpr int kScanCols = 16;
 constexpr int kScanBlocks = kD / kScanCols;
 
 __global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(ChunkLaunch p) {
+    griddep_wait();
     extern __shared__ float scan_smem[];
     const kda_prefill_args& a = p.a;
     const int H = a.n_heads;
@@ -596,8 +599,7 @@ __global__ void __launch_bounds__(kScanThreads) segment_scan_kernel(ChunkLaunch 
 
 cudaError_t launch_segment_meta(const ChunkLaunch& p, cudaStream_t s) {
     note_launch();
-    segment_meta_kernel<<<1, 32, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(segment_meta_kernel, dim3(1), dim3(32), 0, s, p);
 }
 
 cudaError_t launch_segment_scan(const ChunkLaunch& p, cudaStream_t s) {
@@ -607,8 +609,7 @@ cudaError_t launch_segment_scan(const ChunkLaunch& p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(segment_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     note_launch();
-    segment_scan_kernel<<<(unsigned)blocks, kScanThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(segment_scan_kernel, dim3((unsigned)blocks), dim3(kScanThreads), smem, s, p);
 }
 
 template <int MODE>
@@ -619,8 +620,7 @@ cudaError_t launch_recur_mode(const ChunkLaunch& p, cudaStream_t s) {
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     note_launch();
-    chunk_recur_kernel<MODE><<<(unsigned)blocks, kThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(chunk_recur_kernel<MODE>, dim3((unsigned)blocks), dim3(kThreads), kSmemBytes, s, p);
 }
 
 cudaError_t launch_chunk_recur(const ChunkLaunch& p, cudaStream_t s) {

@@ -55,6 +55,7 @@ struct LocalSmem {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kSimtThreads) simt_local_kernel(ChunkLaunch p) {
+    griddep_wait();
     using R = SimtRec<D>;
     extern __shared__ __align__(16) uint8_t simt_smem[];
     LocalSmem& sm = *reinterpret_cast<LocalSmem*>(simt_smem);
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_local_kernel(ChunkLaunch p)
 // The carry of one (sequence, head): the fp32 state S [D][D] in shared memory.
 template <typename T, int D>
 __global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p) {
+    griddep_wait();
     using R = SimtRec<D>;
     constexpr int G = kSimtThreads / D;      // thread groups over the second index
     extern __shared__ __align__(16) uint8_t simt_smem[];
@@ -253,8 +255,7 @@ cudaError_t launch_simt_pair(const ChunkLaunch& p, cudaStream_t s, bool local) {
                                              (int)smem);
         if (e != cudaSuccess) return e;
         note_launch();
-        simt_local_kernel<T, D><<<(unsigned)items, kSimtThreads, smem, s>>>(p);
-        return cudaGetLastError();
+        return launch_overlapped(simt_local_kernel<T, D>, dim3((unsigned)items), dim3(kSimtThreads), smem, s, p);
     }
     const int64_t chains = (int64_t)p.a.n_seqs * p.a.n_heads;
     if (chains == 0) return cudaSuccess;
@@ -263,8 +264,7 @@ cudaError_t launch_simt_pair(const ChunkLaunch& p, cudaStream_t s, bool local) {
                                          (int)smem);
     if (e != cudaSuccess) return e;
     note_launch();
-    simt_recur_kernel<T, D><<<(unsigned)chains, kSimtThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_overlapped(simt_recur_kernel<T, D>, dim3((unsigned)chains), dim3(kSimtThreads), smem, s, p);
 }
 
 cudaError_t launch_simt(const ChunkLaunch& p, cudaStream_t s, bool local) {

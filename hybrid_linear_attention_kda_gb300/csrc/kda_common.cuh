@@ -33,6 +33,31 @@ __device__ __forceinline__ void flag(uint32_t* status, uint32_t bit) {
 // Counts kernel launches (kda_launch_count); every launcher calls it once per launch.
 void note_launch(int n = 1);
 
+// Launches `kernel` with programmatic stream serialization: its CTAs may be
+// scheduled while the previous kernel in the stream finishes, so its launch
+// latency overlaps that kernel's tail.  Such a kernel calls griddep_wait()
+// before it touches memory: the wait returns once the previous grid has
+// completed and its writes are visible, so stream order is kept.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// The first statement of a kernel started by launch_overlapped (a no-op when
+// the kernel was launched plainly).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Records `message` as this host thread's last error (kda_last_error) and returns status.
 kda_status_t record_error(kda_status_t status, const char* message);
 
