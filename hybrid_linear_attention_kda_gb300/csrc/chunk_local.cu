@@ -119,10 +119,19 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
         float t[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) t[r] = r == jj ? 1.f : 0.f;
+        // columns u in groups of four, read as one 16-byte row piece per row r;
+        // each t[r] still takes its updates in increasing u, and rows are visited
+        // in increasing order, so every t[u] is final when it is used
 #pragma unroll
-        for (int u = 0; u < 15; ++u) {
+        for (int g4 = 0; g4 < 4; ++g4) {
 #pragma unroll
-            for (int r = u + 1; r < 16; ++r) t[r] = fmaf(-A[(o + r) * kC + o + u], t[u], t[r]);
+            for (int r = 4 * g4 + 1; r < 16; ++r) {
+                const float4 a4 = *reinterpret_cast<const float4*>(A + (o + r) * kC + o + 4 * g4);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (4 * g4 + e < r) t[r] = fmaf(-av[e], t[4 * g4 + e], t[r]);
+            }
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tf[(o + r) * kC + o + jj] = t[r];
@@ -147,9 +156,12 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
             const float* Ar = A + (16 * i + rr) * kC + 16 * jb;
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int u = 0; u < 16; u += 2) {
-                a0 = fmaf(Ar[u], Tf[(16 * jb + u) * kC + 16 * jb + cc], a0);
-                a1 = fmaf(Ar[u + 1], Tf[(16 * jb + u + 1) * kC + 16 * jb + cc], a1);
+            for (int u = 0; u < 16; u += 4) {
+                const float4 a4 = *reinterpret_cast<const float4*>(Ar + u);
+                a0 = fmaf(a4.x, Tf[(16 * jb + u) * kC + 16 * jb + cc], a0);
+                a1 = fmaf(a4.y, Tf[(16 * jb + u + 1) * kC + 16 * jb + cc], a1);
+                a0 = fmaf(a4.z, Tf[(16 * jb + u + 2) * kC + 16 * jb + cc], a0);
+                a1 = fmaf(a4.w, Tf[(16 * jb + u + 3) * kC + 16 * jb + cc], a1);
             }
             scr[(m << 8) + tid] = a0 + a1;
         }
@@ -160,9 +172,12 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
             const float* Tr = Tf + (16 * i + rr) * kC + 16 * i;
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int u = 0; u < 16; u += 2) {
-                a0 = fmaf(Tr[u], scr[(m << 8) + (u << 4) + cc], a0);
-                a1 = fmaf(Tr[u + 1], scr[(m << 8) + ((u + 1) << 4) + cc], a1);
+            for (int u = 0; u < 16; u += 4) {
+                const float4 t4 = *reinterpret_cast<const float4*>(Tr + u);
+                a0 = fmaf(t4.x, scr[(m << 8) + (u << 4) + cc], a0);
+                a1 = fmaf(t4.y, scr[(m << 8) + ((u + 1) << 4) + cc], a1);
+                a0 = fmaf(t4.z, scr[(m << 8) + ((u + 2) << 4) + cc], a0);
+                a1 = fmaf(t4.w, scr[(m << 8) + ((u + 3) << 4) + cc], a1);
             }
             Tf[(16 * i + rr) * kC + 16 * jb + cc] = -(a0 + a1);
         }
@@ -338,6 +353,13 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         if (tid == 0) {
             ok = mbar_wait(&ms.bar_load, (uint32_t)(k & 1));
             if (ok) ms.ld_waited += 1;
+            if (ok && k > 0) {
+                // the previous item's W and U~ staging lies where this item's v and
+                // X^T go: once the bulk stores have read it, v may land there (the
+                // wait overlaps the q, k, alpha load instead of ending the last item)
+                bulk_wait_read();
+                issue_load_v(item, ms.info[k & 1]);
+            }
         }
         if (__syncthreads_or(!ok)) {
             ok = false;
@@ -669,11 +691,6 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             bulk_s2g(rec + kRecW, sm + kWst, 16384);
             bulk_s2g(rec + kRecU, sm + kWst + 16384, 16384);
             bulk_commit();
-            // the next item's v lands where W and U~ are staged
-            if (item + step < n_items) {
-                bulk_wait_read();
-                issue_load_v(item + step, ms.info[nb]);
-            }
         }
     }
 
