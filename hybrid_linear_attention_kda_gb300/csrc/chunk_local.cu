@@ -42,7 +42,8 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 256;
-constexpr int kCtasPerSm = 2;              // two co-resident CTAs overlap each other's phases
+constexpr int kCtasPerSm = 2;
+constexpr int kStoreThread = 32;           // issues (and waits for) the W / U~ stores and the v loads after the first              // two co-resident CTAs overlap each other's phases
 // Shared memory of one CTA (1024-aligned base), one item at a time.  Channels are
 // taken in two rounds of 64; round g's q, k and alpha boxes ([64 tokens][64
 // channels], no swizzle) fill region g, which then takes the round's K-slices
@@ -353,13 +354,12 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         if (tid == 0) {
             ok = mbar_wait(&ms.bar_load, (uint32_t)(k & 1));
             if (ok) ms.ld_waited += 1;
-            if (ok && k > 0) {
-                // the previous item's W and U~ staging lies where this item's v and
-                // X^T go: once the bulk stores have read it, v may land there (the
-                // wait overlaps the q, k, alpha load instead of ending the last item)
-                bulk_wait_read();
-                issue_load_v(item, ms.info[k & 1]);
-            }
+        } else if (tid == kStoreThread && k > 0) {
+            // the previous item's W and U~ staging lies where this item's v and
+            // X^T go: once the bulk stores (this thread's) have read it, v may land
+            // there; the wait runs beside thread 0's wait for q, k and alpha
+            bulk_wait_read();
+            issue_load_v(item, ms.info[k & 1]);
         }
         if (__syncthreads_or(!ok)) {
             ok = false;
@@ -687,14 +687,14 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
-        if (tid == 0) {
+        if (tid == kStoreThread) {
             bulk_s2g(rec + kRecW, sm + kWst, 16384);
             bulk_s2g(rec + kRecU, sm + kWst + 16384, 16384);
             bulk_commit();
         }
     }
 
-    if (tid == 0) bulk_wait_all();                     // staged records written out
+    if (tid == 0 || tid == kStoreThread) bulk_wait_all();   // staged records written out
     if (!ok && tid == 0) {
         // let this CTA's own copies and MMAs in flight land (bounded) before
         // shared and tensor memory are released
