@@ -42,8 +42,12 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 256;
-constexpr int kCtasPerSm = 2;
-constexpr int kStoreThread = 32;           // issues (and waits for) the W / U~ stores and the v loads after the first              // two co-resident CTAs overlap each other's phases
+constexpr int kCtasPerSm = 2;              // two co-resident CTAs overlap each other's phases
+// Thread 0 waits on the mbarriers and issues the MMAs.  Two other threads issue
+// the copies, so that a copy engine that is slow to accept work does not hold up
+// thread 0's chain:
+constexpr int kStoreThread = 32;           // the W / U~ stores and, after the first item, the v loads
+constexpr int kLoadThread = 64;            // the P stores and, after the first item, the q, k, alpha loads
 // Shared memory of one CTA (1024-aligned base), one item at a time.  Channels are
 // taken in two rounds of 64; round g's q, k and alpha boxes ([64 tokens][64
 // channels], no swizzle) fill region g, which then takes the round's K-slices
@@ -148,7 +152,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
         side();       // warps 4-7: work of the caller's that does not depend on T
     }
     __syncthreads();
-    if (tid == 0) after_stage1();
+    if (tid == kLoadThread) after_stage1();
     {   // blocks (1,0) and (3,2): M = A_ij T_jj, then T_ij = -T_ii M
         const int rr = tid >> 4, cc = tid & 15;
 #pragma unroll
@@ -657,7 +661,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         fence_after_sync();
         // [0, 64 KiB) is free once the staged P has been read: the next item's
         // q, k and alpha go there now
-        if (tid == 0 && item + step < n_items) {
+        if (tid == kLoadThread && item + step < n_items) {
             bulk_wait_read();
             issue_load_qka(item + step, ms.info[nb]);
         }
@@ -694,7 +698,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         }
     }
 
-    if (tid == 0 || tid == kStoreThread) bulk_wait_all();   // staged records written out
+    if (tid == kStoreThread || tid == kLoadThread) bulk_wait_all();   // staged records written out
     if (!ok && tid == 0) {
         // let this CTA's own copies and MMAs in flight land (bounded) before
         // shared and tensor memory are released
