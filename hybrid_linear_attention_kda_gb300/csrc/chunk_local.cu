@@ -209,12 +209,19 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
         __syncthreads();
 #pragma unroll
         for (int m = 0; m < 4; ++m) acc[m] = 0.f;
+        // T_11 is lower triangular: row r0 + 8m needs the column groups u / 4 <=
+        // (r0 + 8m) / 4 = 2m + (r0 >> 2) only; r0 is the warp index, so the bound
+        // is the same for the whole warp, and the skipped terms are exact zeros
+        const int extra = r0 >> 2;
 #pragma unroll
-        for (int u = 0; u < 32; u += 4) {
+        for (int ug = 0; ug < 8; ++ug) {
+            if (ug > 6 + extra) break;
+            const int u = 4 * ug;
             const float s0 = scr[u * 32 + cc], s1 = scr[(u + 1) * 32 + cc];
             const float s2 = scr[(u + 2) * 32 + cc], s3 = scr[(u + 3) * 32 + cc];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
+                if (ug > 2 * m + extra) continue;
                 const float4 t4 = *reinterpret_cast<const float4*>(Tf + (32 + r0 + 8 * m) * kC + 32 + u);
                 acc[m] = fmaf(t4.x, s0, acc[m]);
                 acc[m] = fmaf(t4.y, s1, acc[m]);
