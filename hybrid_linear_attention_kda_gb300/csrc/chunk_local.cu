@@ -678,19 +678,16 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             const int row = 32 * (warp & 3) + lane;
             const uint32_t col0 = warp < 4 ? 0u : 64u;
             const uint32_t dst = s_base + kWst + (warp < 4 ? 0u : 16384u);
+            uint32_t v[4][16];
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                uint32_t v[2][16];
-                tmem_ld16(tbase + lanebase + col0 + 32 * q2, v[0]);
-                tmem_ld16(tbase + lanebase + col0 + 32 * q2 + 16, v[1]);
-                tmem_wait_ld();
+            for (int q4 = 0; q4 < 4; ++q4) tmem_ld16(tbase + lanebase + col0 + 16 * q4, v[q4]);
+            tmem_wait_ld();
 #pragma unroll
-                for (int e8 = 0; e8 < 4; ++e8) {
-                    float x[8];
+            for (int e8 = 0; e8 < 8; ++e8) {
+                float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[e8 >> 1][8 * (e8 & 1) + e]);
-                    sts16(dst + row64_chunk_off(row, 4 * q2 + e8), pack8(x));
-                }
+                for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[e8 >> 1][8 * (e8 & 1) + e]);
+                sts16(dst + row64_chunk_off(row, e8), pack8(x));
             }
         }
         if (tid < kC) ms.beta[nb][tid] = beta_nx;
