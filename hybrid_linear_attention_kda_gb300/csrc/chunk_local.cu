@@ -65,11 +65,12 @@ constexpr uint32_t kLbo = 1024, kSbo = 2048;
 constexpr uint32_t kAmat = 0;              // A fp32 [64][64]
 constexpr uint32_t kTf = 16384;            // T fp32 [64][64]
 constexpr uint32_t kTscr = 32768;          // block-product scratch, 1024 fp32
-constexpr uint32_t kTm = 36864;            // (T diag(beta))^T bf16, MN-major [s][r]
+constexpr uint32_t kTm = 98304;            // (T diag(beta))^T bf16, MN-major [s][r]; outside [0, 64 KiB)
+                                           // so the next item's q, k, alpha may land while it is read
 constexpr uint32_t kPst = 45056;           // P record tile, staged for its bulk store
 constexpr uint32_t kWst = kSv;             // after the W/U~ MMA: W and U~ record tiles, staged
                                            // over v and X^T, so the next item's q, k, alpha can land
-constexpr uint32_t kMisc = 98304;
+constexpr uint32_t kMisc = kTm + 8192;
 constexpr uint32_t kTmemCols = 128;
 
 struct Misc {
@@ -636,6 +637,13 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
+        // [0, 64 KiB) is free once the staged P has been read (A and T are consumed,
+        // T' lies above it): the next item's q, k and alpha load while this item's
+        // W / U~ product runs
+        if (tid == kLoadThread && item + step < n_items) {
+            bulk_wait_read();
+            issue_load_qka(item + step, ms.info[nb]);
+        }
 
         if (tid == 0) {
             ok = mbar_wait(&ms.bar_v, (uint32_t)(k & 1));
@@ -666,12 +674,6 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             break;
         }
         fence_after_sync();
-        // [0, 64 KiB) is free once the staged P has been read: the next item's
-        // q, k and alpha go there now
-        if (tid == kLoadThread && item + step < n_items) {
-            bulk_wait_read();
-            issue_load_qka(item + step, ms.info[nb]);
-        }
 
         // ------------------------------------------------------------ phase 4: W and U~ to the record
         {
