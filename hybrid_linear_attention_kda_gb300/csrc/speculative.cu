@@ -14,10 +14,11 @@
 //               S <- Diag(alpha_t) S + k_t u_t^T      for t < n_accept,
 //           and writes it back (no reduction is needed: u_t is known).
 //
-// Both use the tile layout of the single-token decode kernel (one CTA per
+// Both keep the single-token decode kernel's per-thread data (one CTA per
 // (sequence, head), the whole state in registers, 16-byte coalesced access) and
 // its arithmetic in the same order, so verify(1) followed by commit(1) gives the
-// decode step's results bit for bit.  All candidate tokens' inputs are staged in
+// decode step's results bit for bit.  Verify groups its threads so that the sums
+// over the state rows stay inside warps: its token loop has no CTA barrier.  All candidate tokens' inputs are staged in
 // shared memory next to the state load, so the token loop waits on no global
 // load.
 #include "kda_common.cuh"
@@ -35,27 +36,46 @@ struct Tile {
     static_assert(LPR * RPW == 32 && RPT * NW * RPW == D, "tile shape");
 };
 
-// Shared memory of one verify CTA: every candidate token's alpha, k, q and v
-// ([T][D] fp32 each), its beta and q.k, staged once next to the state load.
+// Shared memory of one verify CTA, per candidate token: alpha, k, alpha k and
+// alpha q in a padded row layout (four spare floats after every 16 rows, so the
+// eight row groups of a warp read distinct banks), q and v unpadded, beta and
+// q.k.
+template <int D>
+__host__ __device__ constexpr int verify_row_stride() { return D + D / 4; }
 template <int D>
 __host__ __device__ constexpr size_t verify_smem(int T) {
-    return (size_t)T * (4 * D + 2) * sizeof(float);
+    return (size_t)T * (4 * verify_row_stride<D>() + 2 * D + 2) * sizeof(float);
 }
+__device__ __forceinline__ int vpad(int i) { return i + (i >> 4) * 4; }
 
+// The verify CTA keeps the decode kernel's per-thread data: the same state rows
+// and four columns, summed by the same fmaf chains.  It groups the threads
+// differently: warp W holds columns 16W .. 16W+15, and its lane l takes column
+// quad 4W + (l & 3) of decode's row group g = l >> 2 (decode's warp g / RPW,
+// sub-row g % RPW).  The sum over the eight row groups of a column then runs
+// inside one warp, through warp-private shared memory and in decode's order,
+// and the token loop needs no CTA barrier.
 template <typename T, int D, int NT>
 __global__ void __launch_bounds__(NT) verify_kernel(SpecLaunch p) {
     using L = Tile<D, NT>;
-    constexpr int TJ = L::TJ, LPR = L::LPR, RPW = L::RPW, NW = L::NW, RPT = L::RPT;
-    extern __shared__ float dyn[];
+    constexpr int RPW = L::RPW, RPT = L::RPT, NW = L::NW;
+    constexpr int NG = 8;                       // row groups per column quad
+    constexpr int DP = verify_row_stride<D>();
+    constexpr int RED = 2 * NG * 16 + 16;       // one warp's a and b partials, b offset by 144 floats
+    static_assert(NT / (D / 4) == NG, "eight row groups per column quad");
+    static_assert(RPT % 4 == 0, "rows per group in float4 pieces");
+    extern __shared__ __align__(16) float dyn[];
     const int nT = p.T;
-    float* s_a = dyn;                  // [T][D]
-    float* s_k = s_a + nT * D;
-    float* s_q = s_k + nT * D;
+    float* s_a = dyn;                  // [T][DP]
+    float* s_k = s_a + nT * DP;
+    float* s_ka = s_k + nT * DP;
+    float* s_qa = s_ka + nT * DP;
+    float* s_q = s_qa + nT * DP;       // [T][D]
     float* s_v = s_q + nT * D;
     float* s_beta = s_v + nT * D;      // [T]
     float* s_qk = s_beta + nT;         // [T]
-    __shared__ float s_red_a[NW][TJ], s_red_b[NW][TJ];
-    __shared__ __align__(16) float s_u[TJ];
+    __shared__ __align__(16) float s_red[NW][RED];
+    __shared__ __align__(16) float s_uw[NW][16];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t sh = blockIdx.x;           // seq * H + head
@@ -67,43 +87,51 @@ __global__ void __launch_bounds__(NT) verify_kernel(SpecLaunch p) {
         return;
     }
     const float* S = p.pool + ((int64_t)slot * p.H + h) * D * D;
-    const int cq = lane % LPR;
-    const int rbase = warp * (RPT * RPW) + lane / LPR;
+    const int quad = lane & 3;               // column quad within the warp
+    const int g = lane >> 2;                 // decode's row group
+    const int c0 = 16 * warp + 4 * quad;     // first of this lane's four columns
+    const int rfirst = (g / RPW) * (RPT * RPW) + g % RPW;
+    float4 st[RPT];
+#pragma unroll
+    for (int m = 0; m < RPT; ++m)
+        st[m] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rfirst + m * RPW) * D + c0));
 
     // every candidate token's inputs ([n_seqs, T, H, D] rows) first: they are
     // small and return before the state
     for (int e = tid; e < nT * D; e += NT) {
         const int t = e / D, i = e - t * D;
         const int64_t vec = (((int64_t)seq * nT + t) * p.H + h) * D;
-        s_a[e] = p.alpha[vec + i];
-        s_k[e] = Elem<T>::load(static_cast<const T*>(p.k) + vec + i);
-        s_q[e] = Elem<T>::load(static_cast<const T*>(p.q) + vec + i);
+        const float a = p.alpha[vec + i];
+        const float ki = Elem<T>::load(static_cast<const T*>(p.k) + vec + i);
+        const float qi = Elem<T>::load(static_cast<const T*>(p.q) + vec + i);
+        const int ip = t * DP + vpad(i);
+        s_a[ip] = a;
+        s_k[ip] = ki;
+        s_ka[ip] = a * ki;
+        s_qa[ip] = a * qi;
+        s_q[e] = qi;
         s_v[e] = Elem<T>::load(static_cast<const T*>(p.v) + vec + i);
     }
     for (int t = tid; t < nT; t += NT) s_beta[t] = p.beta[((int64_t)seq * nT + t) * p.H + h];
-    float4 st[RPT];
-#pragma unroll
-    for (int m = 0; m < RPT; ++m)
-        st[m] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rbase + m * RPW) * D + 4 * cq));
     __syncthreads();
     for (int t = warp; t < nT; t += NW) {   // q . k of every token, one warp each
         float acc = 0.f;
-        for (int i = lane; i < D; i += 32) acc = fmaf(s_q[t * D + i], s_k[t * D + i], acc);
+        for (int i = lane; i < D; i += 32) acc = fmaf(s_q[t * D + i], s_k[t * DP + vpad(i)], acc);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) s_qk[t] = acc;
     }
+    __syncthreads();
 
+    float* red = s_red[warp];
+    const int col = lane & 15, which = lane >> 4;   // the output this lane finishes
     for (int t = 0; t < nT; ++t) {
-        const float* a_t = s_a + t * D;
-        const float* k_t = s_k + t * D;
-        const float* q_t = s_q + t * D;
+        const int tb = t * DP;
         float pa[4] = {0.f, 0.f, 0.f, 0.f}, pb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
-            const int i = rbase + m * RPW;
-            const float ai = a_t[i];
-            const float ka = ai * k_t[i], qa = ai * q_t[i];
+            const int ip = tb + vpad(rfirst + m * RPW);
+            const float ka = s_ka[ip], qa = s_qa[ip];
             pa[0] = fmaf(ka, st[m].x, pa[0]);
             pa[1] = fmaf(ka, st[m].y, pa[1]);
             pa[2] = fmaf(ka, st[m].z, pa[2]);
@@ -113,46 +141,39 @@ __global__ void __launch_bounds__(NT) verify_kernel(SpecLaunch p) {
             pb[2] = fmaf(qa, st[m].z, pb[2]);
             pb[3] = fmaf(qa, st[m].w, pb[3]);
         }
+        *reinterpret_cast<float4*>(red + g * 16 + 4 * quad) = make_float4(pa[0], pa[1], pa[2], pa[3]);
+        *reinterpret_cast<float4*>(red + 144 + g * 16 + 4 * quad) = make_float4(pb[0], pb[1], pb[2], pb[3]);
+        __syncwarp();
+        // decode's order: each decode warp's sub-rows combined first, then the
+        // warps summed in order from zero
+        float acc = 0.f;
+        const float* rw = red + 144 * which + col;
 #pragma unroll
-        for (int off = LPR; off < 32; off <<= 1) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                pa[c] += __shfl_xor_sync(0xffffffffu, pa[c], off);
-                pb[c] += __shfl_xor_sync(0xffffffffu, pb[c], off);
-            }
+        for (int w = 0; w < NG / RPW; ++w) {
+            float comb = rw[(w * RPW) * 16];
+            if (RPW == 2) comb = comb + rw[(w * RPW + 1) * 16];
+            acc += comb;
         }
-        if (lane < LPR) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                s_red_a[warp][4 * cq + c] = pa[c];
-                s_red_b[warp][4 * cq + c] = pb[c];
-            }
+        const int j = 16 * warp + col;
+        const int64_t vec = (((int64_t)seq * nT + t) * p.H + h) * D;
+        if (which == 0) {
+            const float u = s_beta[t] * (s_v[t * D + j] - acc);
+            s_uw[warp][col] = u;
+            p.u[vec + j] = u;
         }
-        __syncthreads();     // partial sums (and, at t = 0, every q . k) are in
-        if (tid < TJ) {
-            float a = 0.f, b = 0.f;
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                a += s_red_a[w][tid];
-                b += s_red_b[w][tid];
-            }
-            const int64_t vec = (((int64_t)seq * nT + t) * p.H + h) * D;
-            const float u = s_beta[t] * (s_v[t * D + tid] - a);
-            s_u[tid] = u;
-            p.u[vec + tid] = u;
-            Elem<T>::store(static_cast<T*>(p.o) + vec + tid, p.scale * fmaf(u, s_qk[t], b));
-        }
-        __syncthreads();     // u is in; the next token's partial sums may overwrite s_red
-        const float4 u4 = *reinterpret_cast<const float4*>(&s_u[4 * cq]);
+        __syncwarp();
+        if (which == 1) Elem<T>::store(static_cast<T*>(p.o) + vec + j, p.scale * fmaf(s_uw[warp][col], s_qk[t], acc));
+        const float4 u4 = *reinterpret_cast<const float4*>(&s_uw[warp][4 * quad]);
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
-            const int i = rbase + m * RPW;
-            const float ai = a_t[i], ki = k_t[i];
+            const int ip = tb + vpad(rfirst + m * RPW);
+            const float ai = s_a[ip], ki = s_k[ip];
             st[m].x = fmaf(ai, st[m].x, ki * u4.x);
             st[m].y = fmaf(ai, st[m].y, ki * u4.y);
             st[m].z = fmaf(ai, st[m].z, ki * u4.z);
             st[m].w = fmaf(ai, st[m].w, ki * u4.w);
         }
+        __syncwarp();        // the next token's partials and u may overwrite this token's
     }
 }
 
@@ -223,8 +244,12 @@ __global__ void __launch_bounds__(NT) commit_kernel(SpecLaunch p) {
 template <typename T, int D, int NT>
 struct VerifyK {
     static cudaError_t run(const SpecLaunch& p, cudaStream_t s) {
+        const size_t smem = verify_smem<D>(p.T);
+        cudaError_t e = cudaFuncSetAttribute(verify_kernel<T, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
         note_launch();
-        verify_kernel<T, D, NT><<<(unsigned)((int64_t)p.n_seqs * p.H), NT, verify_smem<D>(p.T), s>>>(p);
+        verify_kernel<T, D, NT><<<(unsigned)((int64_t)p.n_seqs * p.H), NT, smem, s>>>(p);
         return cudaGetLastError();
     }
 };

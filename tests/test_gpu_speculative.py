@@ -70,11 +70,12 @@ def test_verify_and_commit_match_the_oracle(kda, cuda_device, dtype, d):
     assert torch.equal(pool[:3], before[:3])                    # other slots untouched
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_verify_one_then_commit_one_is_the_decode_step(kda, cuda_device, dtype):
-    """Same tile layout and arithmetic order as kda_decode_step: bit for bit."""
+def test_verify_one_then_commit_one_is_the_decode_step(kda, cuda_device, dtype, d):
+    """Same per-thread data and arithmetic order as kda_decode_step: bit for bit."""
     dev = cuda_device
-    n, H, d = 16, 4, 128
+    n, H = 16, 4
     S0 = inputs.gen_states(n, H, d, d, 41, std=0.05).to(dev)
     slots = torch.arange(n, dtype=torch.int32, device=dev)
     z = _tokens(n, 1, H, d, 42, 0, dtype)
