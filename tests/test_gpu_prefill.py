@@ -433,6 +433,32 @@ def test_split_chain_matches_oracle_and_resumes(kda, cuda_device):
                 assert rel_rms(fin2[0, h].cpu(), fin[0, h].cpu()) < BF16_STATE_TOL
 
 
+def test_split_chain_resumes_bit_exactly_inside_a_segment_when_the_gates_forget(kda, cuda_device):
+    """The workloads' gates (decay about e^-140 per chunk): every segment boundary's
+    two-chunk tail map is exactly zero, so a boundary state is the tail window run
+    from zero in both the full run and a run resumed inside the previous segment.
+    The resumed run then reproduces the full run bit for bit, outputs, snapshots
+    and final states, although its first segment is shorter."""
+    dev = cuda_device
+    H, d, T = 2, 128, 1 << 18
+    data = inputs.gen_prefill([T], H, d, d, 20271)
+    n_ord = T // 256
+    pool = torch.zeros((n_ord + n_ord, H, d, d), device=dev)
+    table = np.arange(n_ord, dtype=np.int32)[None]
+    o, fin = run_gpu(kda, dev, data, pool=pool, snap_table=table)
+    assert not torch.isnan(o.float()).any() and not torch.isnan(fin).any()
+    for p in (100096, 200192):
+        tail = {key: data[key][p:] for key in ("q", "k", "v", "alpha", "beta")}
+        tail["cu_seqlens"] = torch.tensor([0, T - p], dtype=torch.int32)
+        table2 = np.full((1, n_ord), -1, np.int32)
+        table2[0, p // 256:] = n_ord + np.arange(n_ord - p // 256)
+        o2, fin2 = run_gpu(kda, dev, tail, start_pos=[p], init_slot=[p // 256 - 1], pool=pool,
+                           snap_table=table2)
+        assert torch.equal(o2, o[p:]), p
+        assert torch.equal(fin2, fin), p
+        assert torch.equal(pool[n_ord:2 * n_ord - p // 256], pool[p // 256:n_ord]), p
+
+
 def test_split_and_plain_sequences_in_one_batch(kda, cuda_device):
     """A batch with a split chain beside plain ones: 140,000 tokens (split), a
     3,000-token sequence resumed at position 512 from a pool state, an empty
