@@ -30,6 +30,7 @@ size_t simt_record_bytes(int d) { return (size_t)(4 * 64 * d + 64 * 64 + d) * si
 namespace {
 
 constexpr int kSimtThreads = 256;
+constexpr int kSimtCols = 16;        // value columns per carry CTA
 constexpr int kCB = kDecayCB;            // channels per block in the chunk-local passes
 constexpr int kLd = kDecayLd;
 
@@ -165,14 +166,20 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p) {
     griddep_wait();
     using R = SimtRec<D>;
-    constexpr int G = kSimtThreads / D;      // thread groups over the second index
+    // Every column of S evolves on its own (U, O and the update of column j read
+    // only column j of S and U), so a chain is split over D / kSimtCols CTAs, one
+    // block of value columns each; the arithmetic of every element is unchanged.
+    constexpr int JB = kSimtCols;
+    constexpr int G = kSimtThreads / JB;     // thread groups over the second index
     extern __shared__ __align__(16) uint8_t simt_smem[];
-    float* S = reinterpret_cast<float*>(simt_smem);          // [D][D]
-    float* U = S + D * D;                                    // [64][D]
+    float* S = reinterpret_cast<float*>(simt_smem);          // [D][JB]
+    float* U = S + D * JB;                                   // [64][JB]
     const kda_prefill_args& a = p.a;
     const int H = a.n_heads;
     const int tid = threadIdx.x;
-    const int seq = (int)(blockIdx.x / H), h = (int)(blockIdx.x % H);
+    const int64_t chain = blockIdx.x / (D / JB);
+    const int jb = (int)(blockIdx.x % (D / JB)) * JB;
+    const int seq = (int)(chain / H), h = (int)(chain % H);
     int64_t tb, te, pos0;
     int32_t init;
     uint32_t bad;
@@ -182,10 +189,10 @@ __global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p)
     if (nc < 0 || g0 + nc > p.max_chunks) return;
     const int64_t slot_stride = (int64_t)H * D * D;
     const int64_t head_off = (int64_t)h * D * D;
-    const int j = tid % D, grp = tid / D;
+    const int jl = tid % JB, grp = tid / JB, j = jb + jl;   // this thread's value column
 
     const float* S0 = init >= 0 ? a.pool + (int64_t)init * slot_stride + head_off : nullptr;
-    for (int e = tid; e < D * D; e += kSimtThreads) S[e] = S0 ? S0[e] : 0.f;
+    for (int e = tid; e < D * JB; e += kSimtThreads) S[e] = S0 ? S0[(e / JB) * D + jb + e % JB] : 0.f;
     T* o = static_cast<T*>(a.o);
 
     for (int64_t lc = 0; lc < nc; ++lc) {
@@ -197,8 +204,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p)
         for (int t = grp; t < n; t += G) {
             const float* w = rec + R::W + t * D;
             float acc = rec[R::U + t * D + j];
-            for (int c = 0; c < D; ++c) acc = fmaf(-w[c], S[c * D + j], acc);
-            U[t * D + j] = acc;
+            for (int c = 0; c < D; ++c) acc = fmaf(-w[c], S[c * JB + jl], acc);
+            U[t * JB + jl] = acc;
         }
         __syncthreads();
         // O = Q~ S + P U
@@ -206,16 +213,16 @@ __global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p)
             const float* qt = rec + R::Q + t * D;
             const float* pt = rec + R::P + t * 64;
             float acc = 0.f;
-            for (int c = 0; c < D; ++c) acc = fmaf(qt[c], S[c * D + j], acc);
-            for (int s = 0; s <= t; ++s) acc = fmaf(pt[s], U[s * D + j], acc);
+            for (int c = 0; c < D; ++c) acc = fmaf(qt[c], S[c * JB + jl], acc);
+            for (int s = 0; s <= t; ++s) acc = fmaf(pt[s], U[s * JB + jl], acc);
             Elem<T>::store(o + ((t0 + t) * H + h) * D + j, a.scale * acc);
         }
         __syncthreads();                                         // every read of S done
         // S <- Diag(gamma) S + Kbar^T U
         for (int c = grp; c < D; c += G) {
-            float acc = rec[R::G + c] * S[c * D + j];
-            for (int t = 0; t < n; ++t) acc = fmaf(rec[R::K + t * D + c], U[t * D + j], acc);
-            S[c * D + j] = acc;
+            float acc = rec[R::G + c] * S[c * JB + jl];
+            for (int t = 0; t < n; ++t) acc = fmaf(rec[R::K + t * D + c], U[t * JB + jl], acc);
+            S[c * JB + jl] = acc;
         }
         // a snapshot after this chunk
         const int64_t p_end = pos0 + lc * kC + n;
@@ -223,25 +230,25 @@ __global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p)
             const int64_t ord = p_end / a.snap_interval - 1;
             int32_t slot = -1;
             if (ord >= a.snap_table_stride) {
-                if (tid == 0) flag(p.status, KDA_DEV_BAD_ORDINAL);
+                if (tid == 0 && jb == 0) flag(p.status, KDA_DEV_BAD_ORDINAL);
             } else {
                 slot = a.snap_table[(int64_t)seq * a.snap_table_stride + ord];
                 if (slot != -1 && (slot < 0 || (int64_t)slot >= a.n_slots)) {
-                    if (tid == 0) flag(p.status, KDA_DEV_BAD_SLOT);
+                    if (tid == 0 && jb == 0) flag(p.status, KDA_DEV_BAD_SLOT);
                     slot = -1;
                 }
             }
             if (slot >= 0) {
                 __syncthreads();
                 float* dst = a.pool + (int64_t)slot * slot_stride + head_off;
-                for (int e = tid; e < D * D; e += kSimtThreads) dst[e] = S[e];
+                for (int e = tid; e < D * JB; e += kSimtThreads) dst[(e / JB) * D + jb + e % JB] = S[e];
             }
         }
     }
     __syncthreads();
     if (a.final_state) {
         float* dst = a.final_state + (int64_t)seq * slot_stride + head_off;
-        for (int e = tid; e < D * D; e += kSimtThreads) dst[e] = S[e];
+        for (int e = tid; e < D * JB; e += kSimtThreads) dst[(e / JB) * D + jb + e % JB] = S[e];
     }
 }
 
@@ -259,12 +266,13 @@ cudaError_t launch_simt_pair(const ChunkLaunch& p, cudaStream_t s, bool local) {
     }
     const int64_t chains = (int64_t)p.a.n_seqs * p.a.n_heads;
     if (chains == 0) return cudaSuccess;
-    const size_t smem = (size_t)(D * D + 64 * D) * sizeof(float);
+    const size_t smem = (size_t)(D * kSimtCols + 64 * kSimtCols) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(simt_recur_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     note_launch();
-    return launch_overlapped(simt_recur_kernel<T, D>, dim3((unsigned)chains), dim3(kSimtThreads), smem, s, p);
+    return launch_overlapped(simt_recur_kernel<T, D>, dim3((unsigned)(chains * (D / kSimtCols))), dim3(kSimtThreads),
+                             smem, s, p);
 }
 
 cudaError_t launch_simt(const ChunkLaunch& p, cudaStream_t s, bool local) {
