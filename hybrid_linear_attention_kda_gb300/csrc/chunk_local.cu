@@ -98,6 +98,21 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
 }
 __device__ __forceinline__ void sts16(uint32_t saddr, uint4 v) { st_shared_v4(saddr, v.x, v.y, v.z, v.w); }
 __device__ __forceinline__ void stg16(uint8_t* gaddr, uint4 v) { *reinterpret_cast<uint4*>(gaddr) = v; }
+// A lane's 16 tokens (chunks 2 qq and 2 qq + 1) of record row `row` in the
+// 128-byte-swizzled [row][64 tokens] tile: the two chunks land in one aligned
+// 32-byte pair of the row, in swapped order when bit 0 of the row's swizzle is
+// set, and leave as one 32-byte store (a full sector per lane).
+__device__ __forceinline__ void stg_row_pair(uint8_t* tile, uint32_t row, uint32_t qq, const uint32_t (&lo)[4],
+                                             const uint32_t (&hi)[4]) {
+    const uint32_t x = row & 7u;
+    uint8_t* dst = tile + (row >> 3) * 1024u + x * 128u + (((2u * qq) ^ (x & 6u)) << 4);
+    const bool sw = (x & 1u) != 0;
+    const uint32_t a0 = sw ? hi[0] : lo[0], a1 = sw ? hi[1] : lo[1], a2 = sw ? hi[2] : lo[2], a3 = sw ? hi[3] : lo[3];
+    const uint32_t b0 = sw ? lo[0] : hi[0], b1 = sw ? lo[1] : hi[1], b2 = sw ? lo[2] : hi[2], b3 = sw ? lo[3] : hi[3];
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3), "r"(b0), "r"(b1), "r"(b2), "r"(b3)
+                 : "memory");
+}
 // two bf16 (low half the even token) times two bf16 factors, rounded once
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t x, uint32_t f) {
     uint32_t r;
@@ -427,20 +442,20 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             // tokens (2j, 2j+1) of one channel is scaled by one packed multiply.
             {   // forward: Gamma -> Q~ (record), X^T = Gamma k
                 float G = before;
-                uint32_t gq[4], xk[4];
+                uint32_t gq[2][4], xk[4];
 #pragma unroll
                 for (int i = 0; i < 16; i += 2) {
                     const float G0 = G * al[i];
                     G = G0 * al[i + 1];
                     const uint32_t f = pack_bf16(G0, G);
-                    gq[(i & 7) >> 1] = mul_bf16x2(qp[i >> 1], f);
+                    gq[i >> 3][(i & 7) >> 1] = mul_bf16x2(qp[i >> 1], f);
                     xk[(i & 7) >> 1] = mul_bf16x2(kp[i >> 1], f);
                     if ((i & 7) == 6) {
                         const uint32_t r0 = r_base + (i & ~7);
-                        stg16(rec + kRecQ + row64_chunk_off(c, r0 >> 3), make_uint4(gq[0], gq[1], gq[2], gq[3]));
                         sts16(s_base + kX + row64_chunk_off(c, r0 >> 3), make_uint4(xk[0], xk[1], xk[2], xk[3]));
                     }
                 }
+                stg_row_pair(rec + kRecQ, c, qq, gq[0], gq[1]);
             }
             if (sub) {   // up from the half's reference token: phi = E, psi = 1/E
                 float E = 1.f;
@@ -465,24 +480,21 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             }
             {   // backward: kappa -> Kbar (record); half 0 also xi
                 float Qa = after, Qx = xi_rest;     // the suffix product times the factor beyond the quarter
-                uint32_t kb[4], kx[4];
+                uint32_t kb[2][4], kx[4];
 #pragma unroll
                 for (int i = 14; i >= 0; i -= 2) {
                     const float a1 = Qa, x1 = Qx;   // token i + 1
                     Qa *= al[i + 1];
-                    kb[(i & 7) >> 1] = mul_bf16x2(kp[i >> 1], pack_bf16(Qa, a1));
+                    kb[i >> 3][(i & 7) >> 1] = mul_bf16x2(kp[i >> 1], pack_bf16(Qa, a1));
                     if (!hh) {
                         Qx *= al[i + 1];
                         kx[(i & 7) >> 1] = mul_bf16x2(kp[i >> 1], pack_bf16(Qx, x1));
                         Qx *= al[i];
                     }
                     Qa *= al[i];
-                    if ((i & 7) == 0) {
-                        const uint32_t r0 = r_base + i;
-                        stg16(rec + kRecK + row64_chunk_off(c, r0 >> 3), make_uint4(kb[0], kb[1], kb[2], kb[3]));
-                        if (!hh) sts16(apa + mn_chunk(64 + r0, cl), make_uint4(kx[0], kx[1], kx[2], kx[3]));
-                    }
+                    if ((i & 7) == 0 && !hh) sts16(apa + mn_chunk(64 + r_base + i, cl), make_uint4(kx[0], kx[1], kx[2], kx[3]));
                 }
+                stg_row_pair(rec + kRecK, c, qq, kb[0], kb[1]);
             }
             if (!sub) {  // down to the half's reference token: phi = 1/D, psi = D
                 float D = 1.f;
