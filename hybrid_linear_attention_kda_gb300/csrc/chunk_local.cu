@@ -64,7 +64,7 @@ constexpr uint32_t kLbo = 1024, kSbo = 2048;
 // [0, 64 KiB) once the A/P MMA has read its operands:
 constexpr uint32_t kAmat = 0;              // A fp32 [64][64]
 constexpr uint32_t kTf = 16384;            // T fp32 [64][64]
-constexpr uint32_t kTscr = 32768;          // block-product scratch, 1024 fp32
+constexpr uint32_t kTscr = 32768;          // block-product scratch, 1536 fp32
 constexpr uint32_t kTm = 98304;            // (T diag(beta))^T bf16, MN-major [s][r]; outside [0, 64 KiB)
                                            // so the next item's q, k, alpha may land while it is read
 constexpr uint32_t kPst = 45056;           // P record tile, staged for its bulk store
@@ -126,15 +126,25 @@ __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
 }
 
 // T = (I + A)^-1 for a strictly lower triangular 64 x 64 A (fp32, row-major),
-// by blocks: the four 16 x 16 diagonal blocks by forward substitution, the two
-// 16 x 16 blocks below them inside each 32 x 32 diagonal block, then the lower
-// left 32 x 32 block, each off-diagonal block as
-//     T_ij = -T_ii (A_ij T_jj)       (for the block partition at that level).
-// All 256 threads take part; T (zeros above the diagonal inside the diagonal
-// blocks) goes to Tf, row-major.  scr holds 1024 floats.  Ends with a barrier.
+// by blocks, with T's 16 x 16 blocks T_ij and A's blocks A_ij:
+//   stage 1  the four diagonal blocks T_ii by forward substitution (warps 0-1;
+//            warps 4-7 run the caller's side work);
+//   stage 2  T_10 = -T_11 (A_10 T_00) on warps 0 and 2, T_32 = -T_33 (A_32 T_22)
+//            on warps 1 and 3 (each pair meets at a named barrier between its two
+//            products), while warps 4-7 form the parts of M = A_LL T_00(32) that
+//            need only diagonal blocks: A_L0 T_00 (M's columns 0-15, first term)
+//            and A_L1 T_11 (columns 16-31), with A_LL = [A_L0 | A_L1] the lower-left
+//            32 x 32 block of A;
+//   stage 3  M's columns 0-15 += A_L1 T_10;
+//   stage 4  T_LL = -T_11(32) M, skipping the zero column groups of the
+//            triangular T_11(32) with a bound uniform per warp.
+// T's entries above the diagonal are never written and never read; T' reads
+// T[r][s] for r >= s only.  scr holds 1536 floats: M (32 x 32) and two 16 x 16
+// scratch blocks.  Ends with a barrier.
 template <class Side, class AfterStage1>
 __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, float* scr, int tid, Side side,
                                                   AfterStage1 after_stage1) {
+    const int warp = tid >> 5, lane = tid & 31;
     if (tid < kC) {
         const int o = 16 * (tid >> 4), jj = tid & 15;
         float t[16];
@@ -156,75 +166,106 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tf[(o + r) * kC + o + jj] = t[r];
-    } else if (tid < 2 * kC) {
-        // blocks (0,1) and (2,3) are zero; the 32 x 32 level reads them
-        const int e = tid - kC, b = e >> 5, x = e & 31;       // 2 blocks x 256 entries, 8 per thread
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const int idx = x + 32 * m, rr = idx >> 4, cc = idx & 15;
-            Tf[(32 * b + rr) * kC + 32 * b + 16 + cc] = 0.f;
-        }
-    } else {
+    } else if (tid >= 2 * kC) {
         side();       // warps 4-7: work of the caller's that does not depend on T
     }
     __syncthreads();
     if (tid == kLoadThread) after_stage1();
-    {   // blocks (1,0) and (3,2): M = A_ij T_jj, then T_ij = -T_ii M
-        const int rr = tid >> 4, cc = tid & 15;
+    float* M = scr;                      // [32][32]: rows 32..63 of A, columns 0..31 of T
+    if (warp < 4) {
+        // stage 2: warp pair (b, b + 2) forms T_ij, (i, j) = (1, 0) for b = 0, (3, 2) for b = 1
+        const int b = warp & 1, pt = (warp >> 1) * 32 + lane;         // 0..63 within the pair
+        const int i = 2 * b + 1, j = 2 * b;
+        float* X = scr + 1024 + 256 * b;                              // [16][16]
+        const int r = pt >> 2, c = 4 * (pt & 3);                      // four outputs X[r][c .. c+3]
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* ar = A + (16 * i + r) * kC + 16 * j;
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const int i = 1 + 2 * m, jb = i - 1;
-            const float* Ar = A + (16 * i + rr) * kC + 16 * jb;
-            float a0 = 0.f, a1 = 0.f;
+        for (int u4 = 0; u4 < 4; ++u4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(ar + 4 * u4);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-            for (int u = 0; u < 16; u += 4) {
-                const float4 a4 = *reinterpret_cast<const float4*>(Ar + u);
-                a0 = fmaf(a4.x, Tf[(16 * jb + u) * kC + 16 * jb + cc], a0);
-                a1 = fmaf(a4.y, Tf[(16 * jb + u + 1) * kC + 16 * jb + cc], a1);
-                a0 = fmaf(a4.z, Tf[(16 * jb + u + 2) * kC + 16 * jb + cc], a0);
-                a1 = fmaf(a4.w, Tf[(16 * jb + u + 3) * kC + 16 * jb + cc], a1);
+            for (int e = 0; e < 4; ++e) {
+                const float4 t4 = *reinterpret_cast<const float4*>(Tf + (16 * j + 4 * u4 + e) * kC + 16 * j + c);
+                acc.x = fmaf(av[e], t4.x, acc.x);
+                acc.y = fmaf(av[e], t4.y, acc.y);
+                acc.z = fmaf(av[e], t4.z, acc.z);
+                acc.w = fmaf(av[e], t4.w, acc.w);
             }
-            scr[(m << 8) + tid] = a0 + a1;
         }
-        __syncthreads();
+        *reinterpret_cast<float4*>(X + r * 16 + c) = acc;
+        // the pair's X is complete (named barriers 1 and 2, one per pair)
+        if (b == 0) asm volatile("bar.sync 1, 64;" ::: "memory");
+        else asm volatile("bar.sync 2, 64;" ::: "memory");
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* tr = Tf + (16 * i + r) * kC + 16 * i;
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const int i = 1 + 2 * m, jb = i - 1;
-            const float* Tr = Tf + (16 * i + rr) * kC + 16 * i;
-            float a0 = 0.f, a1 = 0.f;
+        for (int u4 = 0; u4 < 4; ++u4) {
+            const float4 t4 = *reinterpret_cast<const float4*>(tr + 4 * u4);
+            const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
 #pragma unroll
-            for (int u = 0; u < 16; u += 4) {
-                const float4 t4 = *reinterpret_cast<const float4*>(Tr + u);
-                a0 = fmaf(t4.x, scr[(m << 8) + (u << 4) + cc], a0);
-                a1 = fmaf(t4.y, scr[(m << 8) + ((u + 1) << 4) + cc], a1);
-                a0 = fmaf(t4.z, scr[(m << 8) + ((u + 2) << 4) + cc], a0);
-                a1 = fmaf(t4.w, scr[(m << 8) + ((u + 3) << 4) + cc], a1);
+            for (int e = 0; e < 4; ++e) {
+                const float4 x4 = *reinterpret_cast<const float4*>(X + (4 * u4 + e) * 16 + c);
+                acc.x = fmaf(tv[e], x4.x, acc.x);
+                acc.y = fmaf(tv[e], x4.y, acc.y);
+                acc.z = fmaf(tv[e], x4.z, acc.z);
+                acc.w = fmaf(tv[e], x4.w, acc.w);
             }
-            Tf[(16 * i + rr) * kC + 16 * jb + cc] = -(a0 + a1);
         }
-        __syncthreads();
+        *reinterpret_cast<float4*>(Tf + (16 * i + r) * kC + 16 * j + c) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    } else {
+        // stage 2, beside it: M[r][8 cg .. 8 cg + 7] for column groups 0-1 (A_L0 T_00)
+        // and 2-3 (A_L1 T_11), each a 16-term product with one row piece of A
+        const int tc = tid - 4 * 32, r = tc >> 2, cg = tc & 3, blk = cg >> 1;
+        const float* ar = A + (32 + r) * kC + 16 * blk;
+        const float* tb = Tf + (16 * blk) * kC + 16 * blk + 8 * (cg & 1);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(ar + 4 * u4);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 t0 = *reinterpret_cast<const float4*>(tb + (4 * u4 + e) * kC);
+                const float4 t1 = *reinterpret_cast<const float4*>(tb + (4 * u4 + e) * kC + 4);
+                acc[0] = fmaf(av[e], t0.x, acc[0]);
+                acc[1] = fmaf(av[e], t0.y, acc[1]);
+                acc[2] = fmaf(av[e], t0.z, acc[2]);
+                acc[3] = fmaf(av[e], t0.w, acc[3]);
+                acc[4] = fmaf(av[e], t1.x, acc[4]);
+                acc[5] = fmaf(av[e], t1.y, acc[5]);
+                acc[6] = fmaf(av[e], t1.z, acc[6]);
+                acc[7] = fmaf(av[e], t1.w, acc[7]);
+            }
+        }
+        *reinterpret_cast<float4*>(M + r * 32 + 8 * cg) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4*>(M + r * 32 + 8 * cg + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
-    {   // lower-left 32 x 32 block: M = A_LL T_00(32), then T_LL = -T_11(32) M
+    __syncthreads();
+    {   // stage 3: M[r][c], c < 16, += sum_u A_L1[r][u] T_10[u][c]  (two outputs a thread)
+        const int r = tid >> 3, c = 2 * (tid & 7);
+        const float* ar = A + (32 + r) * kC + 16;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(ar + 4 * u4);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 t2 = *reinterpret_cast<const float2*>(Tf + (16 + 4 * u4 + e) * kC + c);
+                a0 = fmaf(av[e], t2.x, a0);
+                a1 = fmaf(av[e], t2.y, a1);
+            }
+        }
+        float2* m2 = reinterpret_cast<float2*>(M + r * 32 + c);
+        const float2 mv = *m2;
+        *m2 = make_float2(mv.x + a0, mv.y + a1);
+    }
+    __syncthreads();
+    {   // stage 4: T_LL = -T_11(32) M
         const int cc = tid & 31, r0 = tid >> 5;       // rows r0, r0 + 8, r0 + 16, r0 + 24
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int u = 0; u < 32; u += 4) {
-            const float t0 = Tf[u * kC + cc], t1 = Tf[(u + 1) * kC + cc];
-            const float t2 = Tf[(u + 2) * kC + cc], t3 = Tf[(u + 3) * kC + cc];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float4 a4 = *reinterpret_cast<const float4*>(A + (32 + r0 + 8 * m) * kC + u);
-                acc[m] = fmaf(a4.x, t0, acc[m]);
-                acc[m] = fmaf(a4.y, t1, acc[m]);
-                acc[m] = fmaf(a4.z, t2, acc[m]);
-                acc[m] = fmaf(a4.w, t3, acc[m]);
-            }
-        }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) scr[(r0 + 8 * m) * 32 + cc] = acc[m];
-        __syncthreads();
-#pragma unroll
-        for (int m = 0; m < 4; ++m) acc[m] = 0.f;
         // T_11 is lower triangular: row r0 + 8m needs the column groups u / 4 <=
         // (r0 + 8m) / 4 = 2m + (r0 >> 2) only; r0 is the warp index, so the bound
         // is the same for the whole warp, and the skipped terms are exact zeros
