@@ -47,8 +47,7 @@ constexpr int kCtasPerSm = 2;              // two co-resident CTAs overlap each 
 // the copies, so that a copy engine that is slow to accept work does not hold up
 // thread 0's chain:
 constexpr int kStoreThread = 32;           // the W / U~ stores and, after the first item, the v loads
-constexpr int kLoadThread = 224;          // warp 7: the P stores (issued while warps 0-1 still invert)
-                                           // and, after the first item, the q, k, alpha loads
+constexpr int kLoadThread = 224;           // the P stores and, after the first item, the q, k, alpha loads
 // Shared memory of one CTA (1024-aligned base), one item at a time.  Channels are
 // taken in two rounds of 64; round g's q, k and alpha boxes ([64 tokens][64
 // channels], no swizzle) fill region g, which then takes the round's K-slices
@@ -63,9 +62,10 @@ constexpr uint32_t kLoadBytes = 65536;     // q, k and alpha of one item
 constexpr uint32_t kVBytes = 16384;        // its v
 constexpr uint32_t kLbo = 1024, kSbo = 2048;
 // [0, 64 KiB) once the A/P MMA has read its operands:
-constexpr uint32_t kAmat = 0;              // A fp32 [64][64]
-constexpr uint32_t kTf = 16384;            // T fp32 [64][64]
-constexpr uint32_t kTscr = 32768;          // block-product scratch, 1536 fp32
+constexpr int kAP = 68;                    // row stride (floats) of A and T: rows 4 banks apart
+constexpr uint32_t kAmat = 0;              // A fp32 [64][kAP]
+constexpr uint32_t kTf = 17408;            // T fp32 [64][kAP]
+constexpr uint32_t kTscr = 34816;          // block-product scratch, 1536 fp32
 constexpr uint32_t kTm = 98304;            // (T diag(beta))^T bf16, MN-major [s][r]; outside [0, 64 KiB)
                                            // so the next item's q, k, alpha may land while it is read
 constexpr uint32_t kPst = 45056;           // P record tile, staged for its bulk store
@@ -88,7 +88,6 @@ struct Misc {
 };
 constexpr size_t kSmemBytes = kMisc + sizeof(Misc) + 1024;
 static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
-static_assert(kLoadThread >= 128 && kLoadThread < kThreads, "the P stores follow warps 4-7's barrier");
 
 struct LocalMaps {
     CUtensorMap q, k, v, alpha;   // 2-D views [T_tot rows x H*128 elements]
@@ -127,11 +126,10 @@ __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
     return (k >> 3) * kSbo + (mn >> 6) * kLbo + (k & 7u) * 128u + ((((mn & 63u) >> 3) ^ (k & 7u)) << 4);
 }
 
-// T = (I + A)^-1 for a strictly lower triangular 64 x 64 A (fp32, row-major),
+// T = (I + A)^-1 for a strictly lower triangular 64 x 64 A (fp32, rows kAP floats apart),
 // by blocks, with T's 16 x 16 blocks T_ij and A's blocks A_ij:
 //   stage 1  the four diagonal blocks T_ii by forward substitution (warps 0-1;
-//            warps 4-7 run the caller's side work, then meet at named barrier 3
-//            and thread kLoadThread, one of them, runs after_stage1);
+//            warps 4-7 run the caller's side work);
 //   stage 2  T_10 = -T_11 (A_10 T_00) on warps 0 and 2, T_32 = -T_33 (A_32 T_22)
 //            on warps 1 and 3 (each pair meets at a named barrier between its two
 //            products), while warps 4-7 form the parts of M = A_LL T_00(32) that
@@ -160,7 +158,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
         for (int g4 = 0; g4 < 4; ++g4) {
 #pragma unroll
             for (int r = 4 * g4 + 1; r < 16; ++r) {
-                const float4 a4 = *reinterpret_cast<const float4*>(A + (o + r) * kC + o + 4 * g4);
+                const float4 a4 = *reinterpret_cast<const float4*>(A + (o + r) * kAP + o + 4 * g4);
                 const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
@@ -168,7 +166,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
             }
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Tf[(o + r) * kC + o + jj] = t[r];
+        for (int r = 0; r < 16; ++r) Tf[(o + r) * kAP + o + jj] = t[r];
     } else if (tid >= 2 * kC) {
         side();       // warps 4-7: work of the caller's that does not depend on T
         // warps 4-7's side work is complete: the caller's follow-up runs on one
@@ -185,14 +183,14 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
         float* X = scr + 1024 + 256 * b;                              // [16][16]
         const int r = pt >> 2, c = 4 * (pt & 3);                      // four outputs X[r][c .. c+3]
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* ar = A + (16 * i + r) * kC + 16 * j;
+        const float* ar = A + (16 * i + r) * kAP + 16 * j;
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
             const float4 a4 = *reinterpret_cast<const float4*>(ar + 4 * u4);
             const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float4 t4 = *reinterpret_cast<const float4*>(Tf + (16 * j + 4 * u4 + e) * kC + 16 * j + c);
+                const float4 t4 = *reinterpret_cast<const float4*>(Tf + (16 * j + 4 * u4 + e) * kAP + 16 * j + c);
                 acc.x = fmaf(av[e], t4.x, acc.x);
                 acc.y = fmaf(av[e], t4.y, acc.y);
                 acc.z = fmaf(av[e], t4.z, acc.z);
@@ -204,7 +202,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
         if (b == 0) asm volatile("bar.sync 1, 64;" ::: "memory");
         else asm volatile("bar.sync 2, 64;" ::: "memory");
         acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* tr = Tf + (16 * i + r) * kC + 16 * i;
+        const float* tr = Tf + (16 * i + r) * kAP + 16 * i;
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
             const float4 t4 = *reinterpret_cast<const float4*>(tr + 4 * u4);
@@ -218,14 +216,14 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
                 acc.w = fmaf(tv[e], x4.w, acc.w);
             }
         }
-        *reinterpret_cast<float4*>(Tf + (16 * i + r) * kC + 16 * j + c) =
+        *reinterpret_cast<float4*>(Tf + (16 * i + r) * kAP + 16 * j + c) =
             make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     } else {
         // stage 2, beside it: M[r][8 cg .. 8 cg + 7] for column groups 0-1 (A_L0 T_00)
         // and 2-3 (A_L1 T_11), each a 16-term product with one row piece of A
         const int tc = tid - 4 * 32, r = tc >> 2, cg = tc & 3, blk = cg >> 1;
-        const float* ar = A + (32 + r) * kC + 16 * blk;
-        const float* tb = Tf + (16 * blk) * kC + 16 * blk + 8 * (cg & 1);
+        const float* ar = A + (32 + r) * kAP + 16 * blk;
+        const float* tb = Tf + (16 * blk) * kAP + 16 * blk + 8 * (cg & 1);
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
@@ -233,8 +231,8 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
             const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float4 t0 = *reinterpret_cast<const float4*>(tb + (4 * u4 + e) * kC);
-                const float4 t1 = *reinterpret_cast<const float4*>(tb + (4 * u4 + e) * kC + 4);
+                const float4 t0 = *reinterpret_cast<const float4*>(tb + (4 * u4 + e) * kAP);
+                const float4 t1 = *reinterpret_cast<const float4*>(tb + (4 * u4 + e) * kAP + 4);
                 acc[0] = fmaf(av[e], t0.x, acc[0]);
                 acc[1] = fmaf(av[e], t0.y, acc[1]);
                 acc[2] = fmaf(av[e], t0.z, acc[2]);
@@ -251,7 +249,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
     __syncthreads();
     {   // stage 3: M[r][c], c < 16, += sum_u A_L1[r][u] T_10[u][c]  (two outputs a thread)
         const int r = tid >> 3, c = 2 * (tid & 7);
-        const float* ar = A + (32 + r) * kC + 16;
+        const float* ar = A + (32 + r) * kAP + 16;
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
@@ -259,7 +257,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
             const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float2 t2 = *reinterpret_cast<const float2*>(Tf + (16 + 4 * u4 + e) * kC + c);
+                const float2 t2 = *reinterpret_cast<const float2*>(Tf + (16 + 4 * u4 + e) * kAP + c);
                 a0 = fmaf(av[e], t2.x, a0);
                 a1 = fmaf(av[e], t2.y, a1);
             }
@@ -285,7 +283,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 if (ug > 2 * m + extra) continue;
-                const float4 t4 = *reinterpret_cast<const float4*>(Tf + (32 + r0 + 8 * m) * kC + 32 + u);
+                const float4 t4 = *reinterpret_cast<const float4*>(Tf + (32 + r0 + 8 * m) * kAP + 32 + u);
                 acc[m] = fmaf(t4.x, s0, acc[m]);
                 acc[m] = fmaf(t4.y, s1, acc[m]);
                 acc[m] = fmaf(t4.z, s2, acc[m]);
@@ -293,7 +291,7 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
             }
         }
 #pragma unroll
-        for (int m = 0; m < 4; ++m) Tf[(32 + r0 + 8 * m) * kC + cc] = -acc[m];
+        for (int m = 0; m < 4; ++m) Tf[(32 + r0 + 8 * m) * kAP + cc] = -acc[m];
         __syncthreads();
     }
 }
@@ -619,13 +617,13 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int r = r4 + e;
-                        Am[r * kC + s] = (wq == 2 || r > s) ? bb[e] * __uint_as_float(v[4 * e4 + e]) : 0.f;
+                        Am[r * kAP + s] = (wq == 2 || r > s) ? bb[e] * __uint_as_float(v[4 * e4 + e]) : 0.f;
                     }
                 }
             } else {                      // rows 16 hf .. 16 hf + 15, columns 32..63 (above the diagonal)
                 const int s = lane + 32;
 #pragma unroll 8
-                for (int r = 16 * hf; r < 16 * hf + 16; ++r) Am[r * kC + s] = 0.f;
+                for (int r = 16 * hf; r < 16 * hf + 16; ++r) Am[r * kAP + s] = 0.f;
             }
         }
         fence_before_sync();
@@ -687,7 +685,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int r = 8 * cc + e;
-                    x[e] = r >= srow ? Tf[r * kC + srow] * bs : 0.f;
+                    x[e] = r >= srow ? Tf[r * kAP + srow] * bs : 0.f;
                 }
                 sts16(s_base + kTm + row64_chunk_off(srow, cc), pack8(x));
             }
