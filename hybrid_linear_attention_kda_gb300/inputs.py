@@ -16,8 +16,13 @@ Recipe (the value distributions of the layer's serving workloads):
 Every sequence draws from its own stream, ``torch.Generator`` seeded with
 ``seed * 1000003 + seq``, in fixed blocks of 4096 tokens (q, k, v, alpha, beta in
 that order per block), so any batch can be generated piecewise and a sequence's
-values do not depend on the other sequences of its batch.
+values do not depend on the other sequences of its batch.  Large batches draw
+their sequences on a thread pool (torch's CPU kernels release the GIL); each
+sequence still draws from its own generator, so the bytes do not change.
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -29,6 +34,19 @@ def _stream(seed: int, seq: int) -> torch.Generator:
     g = torch.Generator()
     g.manual_seed(int(seed) * 1000003 + int(seq))
     return g
+
+
+def _for_each_sequence(fn, n_seqs, total_tokens):
+    """fn(i) for every sequence i; on a thread pool when the batch is large (each
+    call writes a disjoint slice of the packed outputs)."""
+    workers = min(n_seqs, os.cpu_count() or 1, 32)
+    if workers <= 1 or total_tokens < 4 * BLOCK:
+        for i in range(n_seqs):
+            fn(i)
+        return
+    with ThreadPoolExecutor(workers) as ex:
+        for _ in ex.map(fn, range(n_seqs)):
+            pass
 
 
 def _unit_rows(x: torch.Tensor) -> torch.Tensor:
@@ -63,19 +81,10 @@ def gen_prefill(seq_lens, H, d_k, d_v, seed, dtype=torch.bfloat16, decay="config
     v = torch.empty((T, H, d_v), dtype=dtype, **kw)
     alpha = torch.empty((T, H, d_k), dtype=torch.float32, **kw)
     beta = torch.empty((T, H), dtype=torch.float32, **kw)
-    off = 0
-    for s, L in enumerate(seq_lens):
-        g = _stream(seed, s)
-        for b in range(0, L, BLOCK):
-            n = min(BLOCK, L - b)
-            qb, kb, vb, ab, bb = gen_sequence_block(g, BLOCK, H, d_k, d_v, decay)
-            sl = slice(off + b, off + b + n)
-            q[sl] = qb[:n].to(dtype)
-            k[sl] = kb[:n].to(dtype)
-            v[sl] = vb[:n].to(dtype)
-            alpha[sl] = ab[:n].to(torch.float32)
-            beta[sl] = bb[:n].to(torch.float32)
-        off += L
+    offs = np.concatenate([[0], np.cumsum(seq_lens, dtype=np.int64)]) if seq_lens else [0]
+    dst = {"q": q, "k": k, "v": v, "alpha": alpha, "beta": beta}
+    _for_each_sequence(lambda s: _draw_into(_stream(seed, s), seq_lens[s], H, d_k, d_v, dtype, decay, dst,
+                                            int(offs[s])), len(seq_lens), T)
     cu = torch.zeros(len(seq_lens) + 1, dtype=torch.int32)
     cu[1:] = torch.tensor(np.cumsum(seq_lens), dtype=torch.int32) if seq_lens else cu[1:]
     return {"q": q, "k": k, "v": v, "alpha": alpha, "beta": beta,
@@ -240,10 +249,12 @@ def gen_varlen_resume(n_seqs, H, d_k, d_v, max_len, prefix_len, n_resume, seed,
     packed_lens = [lens[i] - start[i] for i in range(n_seqs)]
     T = sum(packed_lens)
     out = _empty(T, H, d_k, d_v, dtype, pin)
-    off = 0
-    for i in range(n_seqs):
-        L, p = lens[i], start[i]
-        if i in resumed:
+    offs = np.concatenate([[0], np.cumsum(packed_lens, dtype=np.int64)])
+    rs = set(resumed)
+
+    def fill(i):
+        L, p, off = lens[i], start[i], int(offs[i])
+        if i in rs:
             own = _empty(L, H, d_k, d_v, dtype)
             _draw_into(_stream(seed, i), L, H, d_k, d_v, dtype, decay, own, 0)
             shared = min(L, prefix_len)
@@ -252,7 +263,8 @@ def gen_varlen_resume(n_seqs, H, d_k, d_v, max_len, prefix_len, n_resume, seed,
                 out[key][off:off + L - p] = own[key][p:L]
         else:
             _draw_into(_stream(seed, i), L, H, d_k, d_v, dtype, decay, out, off)
-        off += L - p
+
+    _for_each_sequence(fill, n_seqs, T)
     cu = torch.zeros(n_seqs + 1, dtype=torch.int32)
     cu[1:] = torch.tensor(np.cumsum(packed_lens), dtype=torch.int32)
     out.update({"cu_seqlens": cu, "start_pos": torch.tensor(start, dtype=torch.int32),
