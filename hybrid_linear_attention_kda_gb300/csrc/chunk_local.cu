@@ -83,7 +83,8 @@ struct Misc {
     uint64_t bar_mma;
     uint32_t tslot;
     int32_t guard_fail;
-    // copies and MMAs thread 0 issued and waited for, to drain on a timeout
+    // copies and MMAs issued (thread 0, kStoreThread, kLoadThread) and waited for
+    // (thread 0), to drain on a timeout
     uint32_t ld_issued, ld_waited, v_issued, v_waited, mma_issued, mma_waited;
 };
 constexpr size_t kSmemBytes = kMisc + sizeof(Misc) + 1024;
@@ -359,7 +360,7 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
         ms.ld_issued = ms.ld_waited = ms.v_issued = ms.v_waited = ms.mma_issued = ms.mma_waited = 0;
         fence_mbar_init();
     }
-    // thread 0 issues every copy and MMA and counts them, to drain on a timeout:
+    // each issuing thread counts the copies it starts, to drain on a timeout:
     // an item's q, k and alpha, then, once the staging above them has been read,
     // its v on a barrier of its own (the gate products start without it)
     auto issue_load_qka = [&](int64_t item, int4 info) {
