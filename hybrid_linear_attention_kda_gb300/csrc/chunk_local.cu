@@ -140,13 +140,22 @@ __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
 //   stage 3  M's columns 0-15 += A_L1 T_10;
 //   stage 4  T_LL = -T_11(32) M, skipping the zero column groups of the
 //            triangular T_11(32) with a bound uniform per warp.
-// T's entries above the diagonal are never written and never read; T' reads
-// T[r][s] for r >= s only.  scr holds 1536 floats: M (32 x 32) and two 16 x 16
+// T's entries above the diagonal are never written and never read.  Each stage
+// also writes its entries of T' = T diag(beta) into the bf16 MN-major [s][r]
+// operand at tm (stage 1 the diagonal blocks and the zeros above them), so T'
+// is complete at the end.  scr holds 1536 floats: M (32 x 32) and two 16 x 16
 // scratch blocks.  Ends with a barrier.
 template <class Side, class AfterStage1>
 __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, float* scr, int tid, Side side,
-                                                  AfterStage1 after_stage1) {
+                                                  AfterStage1 after_stage1, uint32_t tm, const float* bsm) {
     const int warp = tid >> 5, lane = tid & 31;
+    // entry (r, s) of T' = T diag(beta) into the MN-major [s][r] bf16 operand at tm
+    auto put_tp = [&](int r, int s, float t) {
+        const __nv_bfloat16 x = __float2bfloat16_rn(t * bsm[s]);
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(tm + row64_chunk_off(s, r >> 3) + (r & 7) * 2),
+                     "h"(*reinterpret_cast<const uint16_t*>(&x))
+                     : "memory");
+    };
     if (tid < kC) {
         const int o = 16 * (tid >> 4), jj = tid & 15;
         float t[16];
@@ -168,6 +177,20 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tf[(o + r) * kAP + o + jj] = t[r];
+        // T' row s = o + jj: its 16 entries of this diagonal block, and zeros
+        // for every r below the block (T is lower triangular)
+        const int s = o + jj;
+        const float bs = bsm[s];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = 8 * h2 + e >= jj ? t[8 * h2 + e] * bs : 0.f;
+            sts16(tm + row64_chunk_off(s, (o >> 3) + h2), pack8(x));
+        }
+#pragma unroll
+        for (int cz = 0; cz < 6; ++cz)
+            if (cz < (o >> 3)) sts16(tm + row64_chunk_off(s, cz), make_uint4(0u, 0u, 0u, 0u));
     } else if (tid >= 2 * kC) {
         side();       // warps 4-7: work of the caller's that does not depend on T
         // warps 4-7's side work is complete: the caller's follow-up runs on one
@@ -219,6 +242,10 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
         }
         *reinterpret_cast<float4*>(Tf + (16 * i + r) * kAP + 16 * j + c) =
             make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        put_tp(16 * i + r, 16 * j + c, -acc.x);
+        put_tp(16 * i + r, 16 * j + c + 1, -acc.y);
+        put_tp(16 * i + r, 16 * j + c + 2, -acc.z);
+        put_tp(16 * i + r, 16 * j + c + 3, -acc.w);
     } else {
         // stage 2, beside it: M[r][8 cg .. 8 cg + 7] for column groups 0-1 (A_L0 T_00)
         // and 2-3 (A_L1 T_11), each a 16-term product with one row piece of A
@@ -292,8 +319,16 @@ __device__ __forceinline__ void invert_unit_lower(const float* A, float* Tf, flo
             }
         }
 #pragma unroll
-        for (int m = 0; m < 4; ++m) Tf[(32 + r0 + 8 * m) * kAP + cc] = -acc[m];
+        for (int m = 0; m < 4; ++m) {
+            Tf[(32 + r0 + 8 * m) * kAP + cc] = -acc[m];
+            put_tp(32 + r0 + 8 * m, cc, -acc[m]);
+        }
+        // T' complete for the tensor core (async proxy); TMEM reads of this
+        // item ordered before the MMA issued after the barrier
+        fence_async_smem();
+        fence_before_sync();
         __syncthreads();
+        fence_after_sync();
     }
 }
 
@@ -673,28 +708,10 @@ chunk_local_kernel(const __grid_constant__ ChunkLaunch p, const __grid_constant_
             bulk_s2g(rec + kRecP, sm + kPst, 8192);
             bulk_commit();
         };
+        // T and, beside it, T'^T (row s = beta_s times column s of T), the MN-major
+        // [s][r] operand of the W / U~ product
         invert_unit_lower(reinterpret_cast<const float*>(sm + kAmat), reinterpret_cast<float*>(sm + kTf),
-                          reinterpret_cast<float*>(sm + kTscr), tid, p_to_staging, store_p);
-        {   // T'^T row s = beta_s (column s of T, zero above the diagonal), the MN-major [s][r] operand
-            const float* Tf = reinterpret_cast<const float*>(sm + kTf);
-            const int srow = tid & 63;            // a warp reads 32 consecutive columns of T
-            const float bs = bsm[srow];
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-                const int cc = 2 * (tid >> 6) + q2;
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int r = 8 * cc + e;
-                    x[e] = r >= srow ? Tf[r * kAP + srow] * bs : 0.f;
-                }
-                sts16(s_base + kTm + row64_chunk_off(srow, cc), pack8(x));
-            }
-        }
-        fence_async_smem();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
+                          reinterpret_cast<float*>(sm + kTscr), tid, p_to_staging, store_p, s_base + kTm, bsm);
         // [0, 64 KiB) is free once the staged P has been read (A and T are consumed,
         // T' lies above it): the next item's q, k and alpha load while this item's
         // W / U~ product runs
