@@ -47,7 +47,8 @@ constexpr int kCtasPerSm = 2;              // two co-resident CTAs overlap each 
 // the copies, so that a copy engine that is slow to accept work does not hold up
 // thread 0's chain:
 constexpr int kStoreThread = 32;           // the W / U~ stores and, after the first item, the v loads
-constexpr int kLoadThread = 224;           // the P stores and, after the first item, the q, k, alpha loads
+constexpr int kLoadThread = 224;          // warp 7: the P stores (issued while warps 0-1 still invert)
+                                           // and, after the first item, the q, k, alpha loads
 // Shared memory of one CTA (1024-aligned base), one item at a time.  Channels are
 // taken in two rounds of 64; round g's q, k and alpha boxes ([64 tokens][64
 // channels], no swizzle) fill region g, which then takes the round's K-slices
@@ -89,6 +90,7 @@ struct Misc {
 };
 constexpr size_t kSmemBytes = kMisc + sizeof(Misc) + 1024;
 static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
+static_assert(kLoadThread >= 128 && kLoadThread < kThreads, "the P stores follow warps 4-7's barrier");
 
 struct LocalMaps {
     CUtensorMap q, k, v, alpha;   // 2-D views [T_tot rows x H*128 elements]
@@ -130,7 +132,8 @@ __device__ __forceinline__ uint32_t mn_chunk(uint32_t mn, uint32_t k) {
 // T = (I + A)^-1 for a strictly lower triangular 64 x 64 A (fp32, rows kAP floats apart),
 // by blocks, with T's 16 x 16 blocks T_ij and A's blocks A_ij:
 //   stage 1  the four diagonal blocks T_ii by forward substitution (warps 0-1;
-//            warps 4-7 run the caller's side work);
+//            warps 4-7 run the caller's side work, then meet at named barrier 3
+//            and thread kLoadThread, one of them, runs after_stage1);
 //   stage 2  T_10 = -T_11 (A_10 T_00) on warps 0 and 2, T_32 = -T_33 (A_32 T_22)
 //            on warps 1 and 3 (each pair meets at a named barrier between its two
 //            products), while warps 4-7 form the parts of M = A_LL T_00(32) that
