@@ -54,7 +54,10 @@ constexpr float kGuardMin = 7.888609052210118e-31f;   // 2^-100
 // so a segment's map (A, B) comes from running its chunks from the identity
 // with U~ = 0 (A) and from zero (B); a scan gives every segment's initial state,
 // then all segments run in parallel.
-constexpr int64_t kSegTokens = 65536;
+// 57,344 tokens = 896 chunks: a 2^20-token sequence of 8 heads splits into 19
+// segments, 152 chains, one per SM of a 152-SM GB300, and its longest chain is
+// 896 chunks (65,536-token segments gave 128 chains of 1,024 chunks).
+constexpr int64_t kSegTokens = 57344;
 constexpr int64_t kSegChunks = kSegTokens / kC;
 
 // Upper bound on the segments of a batch (and on the scratch entries of split

@@ -394,10 +394,15 @@ def test_varlen_64_shared_prefix_resume(kda, cuda_device):
 
 # ------------------------------------------------------------------ long chains split into segments
 
+# The segment length of split chains (absolute positions at its multiples are
+# segment boundaries, where a resumed run splits as the full run does).
+SEG_TOKENS = 57344
+
 def test_split_chain_matches_oracle_and_resumes(kda, cuda_device):
     """One sequence of 2^18 tokens, 4 heads, mild decay (the state carried over a
-    segment boundary matters): the chain is split at multiples of 65,536 tokens
-    and the segments run in parallel from scanned start states.  The whole run
+    segment boundary matters): the chain is split at multiples of the library's
+    segment length (57,344 tokens) and the segments run in parallel from scanned
+    start states.  The whole run
     is checked against the oracle; a resume at a segment boundary reproduces the
     full run bit for bit, a resume inside a segment stays within tolerance."""
     dev = cuda_device
@@ -407,7 +412,7 @@ def test_split_chain_matches_oracle_and_resumes(kda, cuda_device):
     pool = torch.zeros((n_ord + n_ord, H, d, d), device=dev)
     table = np.arange(n_ord, dtype=np.int32)[None]
     o, fin = run_gpu(kda, dev, data, pool=pool, snap_table=table)
-    checks = [65536, 100096, 131072, 196608 + 2560]
+    checks = [SEG_TOKENS, 100096, 2 * SEG_TOKENS, 3 * SEG_TOKENS + 2560]
     ref = oracle.run(data["q"], data["k"], data["v"], data["alpha"], data["beta"], [0, T],
                      snap_req=[(0, p // 256 - 1) for p in checks])
     for h in range(H):
@@ -416,7 +421,7 @@ def test_split_chain_matches_oracle_and_resumes(kda, cuda_device):
         for i, p in enumerate(checks):
             assert rel_rms(pool[p // 256 - 1, h].cpu(), ref["snaps"][i, h]) < BF16_STATE_TOL, (p, h)
 
-    for p, exact in ((131072, True), (100096, False)):
+    for p, exact in ((2 * SEG_TOKENS, True), (100096, False)):
         tail = {key: data[key][p:] for key in ("q", "k", "v", "alpha", "beta")}
         tail["cu_seqlens"] = torch.tensor([0, T - p], dtype=torch.int32)
         table2 = np.full((1, n_ord), -1, np.int32)
