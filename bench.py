@@ -163,10 +163,10 @@ def kernel_fingerprint(kernel=None):
 # DRAM bytes per launch of a prefill kernel on this workload from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (kernel, fingerprint
 # of its sources); any other fingerprint reports null.  The capture ran 2 x 8192
-# tokens x 32 heads (8192 items, 1,236.5 MB); chunk_local's traffic grows with
+# tokens x 32 heads (8192 items, 1,236.6 MB); chunk_local's traffic grows with
 # the item count, so the 16,384-item workload here moves twice that.
 RECORDED_TRAFFIC = {
-    ("chunk_local", "2756b26c92d12e5a"): 2 * (673_388_288 + 563_141_120),
+    ("chunk_local", "63eca31be9c9665c"): 2 * (673_399_808 + 563_152_128),
 }
 
 
