@@ -83,6 +83,14 @@ __global__ void __launch_bounds__(NT) fused_decode_kernel(FusedDecodeLaunch L) {
         const int c = tid + NT * j;
         av[j] = c < D ? bf(p.a, vec + c) : 0.f;
     }
+    // the epilogue's inputs too: beta's logit, and per output channel the norm
+    // weight and the output gate's logit
+    const float b_logit = bf(p.b, sh);
+    float nw = 0.f, g_logit = 0.f;
+    if (tid < TJ) {
+        nw = p.norm_w[(int64_t)h * D + tid];
+        g_logit = bf(p.g, vec + tid);
+    }
 
     // then the state, held in registers until the update
     float4 st[RPT];
@@ -171,7 +179,7 @@ __global__ void __launch_bounds__(NT) fused_decode_kernel(FusedDecodeLaunch L) {
             av += s_red_a[w][tid];
             bv += s_red_b[w][tid];
         }
-        const float beta = sigmoidf(bf(p.b, sh));
+        const float beta = sigmoidf(b_logit);
         const float u = beta * (s_y[2][tid] - av);
         s_u[tid] = u;
         o = fmaf(u, qk, bv);
@@ -181,14 +189,7 @@ __global__ void __launch_bounds__(NT) fused_decode_kernel(FusedDecodeLaunch L) {
         if (lane == 0) s_osq[warp] = sq;
     }
     __syncthreads();
-    if (tid < TJ) {
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < TJ / 32; ++w) tot += s_osq[w];
-        const float r = 1.f / sqrtf(tot / (float)TJ + p.norm_eps);
-        const float yj = p.norm_w[(int64_t)h * D + tid] * o * r * sigmoidf(bf(p.g, vec + tid));
-        static_cast<__nv_bfloat16*>(p.y)[vec + tid] = __float2bfloat16_rn(yj);
-    }
+    // the state leaves first, then the gated RMSNorm output
     const float4 u4 = *reinterpret_cast<const float4*>(&s_u[4 * cq]);
 #pragma unroll
     for (int m = 0; m < RPT; ++m) {
@@ -200,6 +201,14 @@ __global__ void __launch_bounds__(NT) fused_decode_kernel(FusedDecodeLaunch L) {
         r.z = fmaf(ai, st[m].z, ki * u4.z);
         r.w = fmaf(ai, st[m].w, ki * u4.w);
         __stcs(reinterpret_cast<float4*>(S + (int64_t)(rbase + m * RPW) * D + 4 * cq), r);
+    }
+    if (tid < TJ) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < TJ / 32; ++w) tot += s_osq[w];
+        const float r = 1.f / sqrtf(tot / (float)TJ + p.norm_eps);
+        const float yj = nw * o * r * sigmoidf(g_logit);
+        static_cast<__nv_bfloat16*>(p.y)[vec + tid] = __float2bfloat16_rn(yj);
     }
 }
 
