@@ -177,22 +177,32 @@ __global__ void __launch_bounds__(NT) verify_kernel(SpecLaunch p) {
     }
 }
 
-// Shared memory of one commit CTA: alpha and k ([T][D]) and u ([T][D]) of the
-// accepted tokens.
+// Shared memory of one commit CTA: alpha and u ([T][D] fp32) and k ([T][D] in
+// its element type, within a [T][D] fp32-sized slot) of the accepted tokens.
 template <int D>
 __host__ __device__ constexpr size_t commit_smem(int T) {
     return (size_t)T * 3 * D * sizeof(float);
 }
 
+// A 16-byte asynchronous copy from global to shared memory: no register holds
+// the data, so a thread's copies are all in flight at once.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(__cvta_generic_to_global(gmem))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 template <typename T, int D, int NT>
 __global__ void __launch_bounds__(NT) commit_kernel(SpecLaunch p) {
     using L = Tile<D, NT>;
     constexpr int LPR = L::LPR, RPW = L::RPW, RPT = L::RPT;
-    extern __shared__ float dyn[];
+    extern __shared__ __align__(16) float dyn[];
     const int nT = p.T;
     float* s_a = dyn;
-    float* s_k = s_a + nT * D;
-    float* s_u = s_k + nT * D;
+    T* s_k = reinterpret_cast<T*>(s_a + nT * D);
+    float* s_u = s_a + 2 * nT * D;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t sh = blockIdx.x;
@@ -212,24 +222,35 @@ __global__ void __launch_bounds__(NT) commit_kernel(SpecLaunch p) {
     float* S = p.pool + ((int64_t)slot * p.H + h) * D * D;
     const int cq = lane % LPR;
     const int rbase = warp * (RPT * RPW) + lane / LPR;
+    // the accepted tokens' alpha, u and k ([n_seqs, T, H, D] rows, 16-byte
+    // aligned) by asynchronous copies, then the state
+    constexpr int F4 = D / 4;                          // 16-byte pieces of an fp32 row
+    constexpr int KP = D * (int)sizeof(T) / 16;        // 16-byte pieces of a k row
+    for (int e = tid; e < m_acc * F4; e += NT) {
+        const int t = e / F4, i = 4 * (e - t * F4);
+        const int64_t vec = (((int64_t)seq * nT + t) * p.H + h) * D;
+        cp_async16(s_a + t * D + i, p.alpha + vec + i);
+        cp_async16(s_u + t * D + i, p.u + vec + i);
+    }
+    for (int e = tid; e < m_acc * KP; e += NT) {
+        const int t = e / KP, i = e - t * KP;
+        const int64_t vec = (((int64_t)seq * nT + t) * p.H + h) * D;
+        cp_async16(reinterpret_cast<uint8_t*>(s_k + t * D) + 16 * i,
+                   reinterpret_cast<const uint8_t*>(static_cast<const T*>(p.k) + vec) + 16 * i);
+    }
+    cp_async_commit();
     float4 st[RPT];
 #pragma unroll
     for (int m = 0; m < RPT; ++m)
         st[m] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rbase + m * RPW) * D + 4 * cq));
-    for (int e = tid; e < m_acc * D; e += NT) {
-        const int t = e / D, i = e - t * D;
-        const int64_t vec = (((int64_t)seq * nT + t) * p.H + h) * D;
-        s_a[e] = p.alpha[vec + i];
-        s_k[e] = Elem<T>::load(static_cast<const T*>(p.k) + vec + i);
-        s_u[e] = p.u[vec + i];
-    }
+    cp_async_wait_all();
     __syncthreads();
     for (int t = 0; t < m_acc; ++t) {
         const float4 u4 = *reinterpret_cast<const float4*>(&s_u[t * D + 4 * cq]);
 #pragma unroll
         for (int m = 0; m < RPT; ++m) {
             const int i = rbase + m * RPW;
-            const float ai = s_a[t * D + i], ki = s_k[t * D + i];
+            const float ai = s_a[t * D + i], ki = Elem<T>::load(s_k + t * D + i);
             st[m].x = fmaf(ai, st[m].x, ki * u4.x);
             st[m].y = fmaf(ai, st[m].y, ki * u4.y);
             st[m].z = fmaf(ai, st[m].z, ki * u4.z);
