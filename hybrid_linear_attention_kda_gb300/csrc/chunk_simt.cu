@@ -200,21 +200,46 @@ __global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p)
         const int n = (int)(te - t0 < kC ? te - t0 : kC);
         const float* rec = reinterpret_cast<const float*>(p.records) + (size_t)((g0 + lc) * H + h) * R::floats;
         __syncthreads();                                         // S complete
-        // U = U~ - W S
+        // U = U~ - W S (record rows read as 16-byte pieces; the sums keep their order)
         for (int t = grp; t < n; t += G) {
-            const float* w = rec + R::W + t * D;
+            const float4* w = reinterpret_cast<const float4*>(rec + R::W + t * D);
             float acc = rec[R::U + t * D + j];
-            for (int c = 0; c < D; ++c) acc = fmaf(-w[c], S[c * JB + jl], acc);
+#pragma unroll
+            for (int c4 = 0; c4 < D / 4; ++c4) {
+                const float4 w4 = w[c4];
+                const float* sc = S + 4 * c4 * JB + jl;
+                acc = fmaf(-w4.x, sc[0], acc);
+                acc = fmaf(-w4.y, sc[JB], acc);
+                acc = fmaf(-w4.z, sc[2 * JB], acc);
+                acc = fmaf(-w4.w, sc[3 * JB], acc);
+            }
             U[t * JB + jl] = acc;
         }
         __syncthreads();
         // O = Q~ S + P U
         for (int t = grp; t < n; t += G) {
-            const float* qt = rec + R::Q + t * D;
+            const float4* qt = reinterpret_cast<const float4*>(rec + R::Q + t * D);
             const float* pt = rec + R::P + t * 64;
             float acc = 0.f;
-            for (int c = 0; c < D; ++c) acc = fmaf(qt[c], S[c * JB + jl], acc);
-            for (int s = 0; s <= t; ++s) acc = fmaf(pt[s], U[s * JB + jl], acc);
+#pragma unroll
+            for (int c4 = 0; c4 < D / 4; ++c4) {
+                const float4 q4 = qt[c4];
+                const float* sc = S + 4 * c4 * JB + jl;
+                acc = fmaf(q4.x, sc[0], acc);
+                acc = fmaf(q4.y, sc[JB], acc);
+                acc = fmaf(q4.z, sc[2 * JB], acc);
+                acc = fmaf(q4.w, sc[3 * JB], acc);
+            }
+            const int full = (t + 1) & ~3;              // P row entries s < full in 16-byte pieces
+            for (int s = 0; s < full; s += 4) {
+                const float4 p4 = *reinterpret_cast<const float4*>(pt + s);
+                const float* us = U + s * JB + jl;
+                acc = fmaf(p4.x, us[0], acc);
+                acc = fmaf(p4.y, us[JB], acc);
+                acc = fmaf(p4.z, us[2 * JB], acc);
+                acc = fmaf(p4.w, us[3 * JB], acc);
+            }
+            for (int s = full; s <= t; ++s) acc = fmaf(pt[s], U[s * JB + jl], acc);
             Elem<T>::store(o + ((t0 + t) * H + h) * D + j, a.scale * acc);
         }
         __syncthreads();                                         // every read of S done
