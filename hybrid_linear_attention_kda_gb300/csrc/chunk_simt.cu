@@ -54,6 +54,54 @@ struct LocalSmem {
     float beta[64];
 };
 
+// The A and P sums of one block of channels, taken by key token: the thread
+// holds the pairs (r, s) with r = rs + 4 m, m = 0..15, of key s, and adds the
+// block's channels to them in channel order, as accumulate_ap does for its
+// pairs.  The factor of a pair is the one pair_decay forms: within s's 16-token
+// group G the left-to-right product alpha_{s+1} ... alpha_r, here the running
+// product as r walks up the group (one multiply per token, no per-pair chain);
+// from a later group, pout_s pin_r times the whole groups between.  G is uniform
+// in a warp, so every accumulator index is known at compile time.
+template <int G>
+__device__ __forceinline__ void accumulate_ap_key_group(const DecayBlock& D, int s, int rs, float (&accA)[16],
+                                                        float (&accP)[16]) {
+    const int us = s & 15;
+#pragma unroll 1
+    for (int c = 0; c < kDecayCB; ++c) {
+        const float ks = D.k[s][c];
+        float f = 1.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int r = 16 * G + u;
+            if (u > us) f *= D.al[r][c];
+            if (u >= us && (u & 3) == rs) {
+                const float e = f * ks;
+                accP[4 * G + (u >> 2)] = fmaf(D.q[r][c], e, accP[4 * G + (u >> 2)]);
+                accA[4 * G + (u >> 2)] = fmaf(D.k[r][c], e, accA[4 * G + (u >> 2)]);
+            }
+        }
+#pragma unroll
+        for (int m = 4 * (G + 1); m < 16; ++m) {
+            const int r = rs + 4 * m;
+            float fx = D.pout[s][c] * D.pin[r][c];
+#pragma unroll
+            for (int b = G + 1; b < (m >> 2); ++b) fx *= D.btot[b][c];
+            const float e = fx * ks;
+            accP[m] = fmaf(D.q[r][c], e, accP[m]);
+            accA[m] = fmaf(D.k[r][c], e, accA[m]);
+        }
+    }
+}
+__device__ __forceinline__ void accumulate_ap_by_key(const DecayBlock& D, int s, int rs, float (&accA)[16],
+                                                     float (&accP)[16]) {
+    switch (s >> 4) {
+        case 0: accumulate_ap_key_group<0>(D, s, rs, accA, accP); break;
+        case 1: accumulate_ap_key_group<1>(D, s, rs, accA, accP); break;
+        case 2: accumulate_ap_key_group<2>(D, s, rs, accA, accP); break;
+        default: accumulate_ap_key_group<3>(D, s, rs, accA, accP); break;
+    }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kSimtThreads) simt_local_kernel(ChunkLaunch p) {
     griddep_wait();
@@ -78,8 +126,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_local_kernel(ChunkLaunch p)
     const T* v = static_cast<const T*>(a.v);
     if (tid < 64) sm.beta[tid] = tid < n ? a.beta[(t0 + tid) * H + h] : 0.f;
 
-    // this thread's 16 (r, s) pairs: row r, columns s = cs + 4 m
-    const int r = tid >> 2, cs = tid & 3;
+    // this thread's 16 (r, s) pairs: key s, rows r = rs + 4 m
+    const int s = tid >> 2, rs = tid & 3;
     float accA[16], accP[16];
 #pragma unroll
     for (int m = 0; m < 16; ++m) accA[m] = accP[m] = 0.f;
@@ -108,12 +156,12 @@ __global__ void __launch_bounds__(kSimtThreads) simt_local_kernel(ChunkLaunch p)
             rec[R::W + t * D + cb + c] = G * D1.k[t][c];
             if (t == 63) rec[R::G + cb + c] = G;
         }
-        accumulate_ap(D1, r, cs, accA, accP);
+        accumulate_ap_by_key(D1, s, rs, accA, accP);
     }
     // A (strictly lower, beta_r scaled) to shared memory; P to the record
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
-        const int s = cs + 4 * m;
+        const int r = rs + 4 * m;
         sm.A[r][s] = s < r ? sm.beta[r] * accA[m] : 0.f;
         rec[R::P + r * 64 + s] = s <= r ? accP[m] : 0.f;
     }
