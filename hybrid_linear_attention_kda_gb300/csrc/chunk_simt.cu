@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_local_kernel(ChunkLaunch p)
         sm.T[j][j] = 1.f;
         for (int i = j + 1; i < 64; ++i) {
             float acc = 0.f;
+#pragma unroll 8
             for (int s = j; s < i; ++s) acc = fmaf(sm.A[i][s], sm.T[s][j], acc);
             sm.T[i][j] = -acc;
         }
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_local_kernel(ChunkLaunch p)
         }
         __syncthreads();
         float w4[4] = {0.f, 0.f, 0.f, 0.f}, u4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
         for (int s = 0; s <= orow; ++s) {
             const float t = sm.T[orow][s];
 #pragma unroll
