@@ -20,6 +20,7 @@
 //
 // Record of one (chunk, head), fp32, token-major rows:
 //   W [64][D], Q~ [64][D], Kbar [64][D], U~ [64][D], P [64][64], gamma [D]
+#include "async_copy.cuh"
 #include "chunk_common.cuh"
 #include "chunk_decay.cuh"
 
@@ -224,6 +225,14 @@ __global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p)
     extern __shared__ __align__(16) uint8_t simt_smem[];
     float* S = reinterpret_cast<float*>(simt_smem);          // [D][JB]
     float* U = S + D * JB;                                   // [64][JB]
+    // the chunk's record, staged: W, Q~, Kbar [64][D] each and P [64][64],
+    // gamma [D] in the record's order, then this CTA's columns of U~ [64][JB]
+    float* sW = U + 64 * JB;
+    float* sQ = sW + 64 * D;
+    float* sK = sQ + 64 * D;
+    float* sP = sK + 64 * D;
+    float* sG = sP + 64 * 64;
+    float* sU = sG + D;
     const kda_prefill_args& a = p.a;
     const int H = a.n_heads;
     const int tid = threadIdx.x;
@@ -249,11 +258,23 @@ __global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p)
         const int64_t t0 = tb + lc * kC;
         const int n = (int)(te - t0 < kC ? te - t0 : kC);
         const float* rec = reinterpret_cast<const float*>(p.records) + (size_t)((g0 + lc) * H + h) * R::floats;
-        __syncthreads();                                         // S complete
-        // U = U~ - W S (record rows read as 16-byte pieces; the sums keep their order)
+        __syncthreads();                                         // S complete, staging free
+        // the record into shared memory by 16-byte asynchronous copies (records
+        // and their rows are 16-byte aligned): W, Q~ and Kbar are one range of the
+        // record, P and gamma another
+        for (int e = tid; e < 3 * 64 * D / 4; e += kSimtThreads) cp_async16(sW + 4 * e, rec + R::W + 4 * e);
+        for (int e = tid; e < (64 * 64 + D) / 4; e += kSimtThreads) cp_async16(sP + 4 * e, rec + R::P + 4 * e);
+        for (int e = tid; e < 64 * JB / 4; e += kSimtThreads) {
+            const int t = e / (JB / 4), i = 4 * (e % (JB / 4));
+            cp_async16(sU + t * JB + i, rec + R::U + t * D + jb + i);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        __syncthreads();
+        // U = U~ - W S (rows read as 16-byte pieces; the sums keep their order)
         for (int t = grp; t < n; t += G) {
-            const float4* w = reinterpret_cast<const float4*>(rec + R::W + t * D);
-            float acc = rec[R::U + t * D + j];
+            const float4* w = reinterpret_cast<const float4*>(sW + t * D);
+            float acc = sU[t * JB + jl];
 #pragma unroll
             for (int c4 = 0; c4 < D / 4; ++c4) {
                 const float4 w4 = w[c4];
@@ -268,8 +289,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p)
         __syncthreads();
         // O = Q~ S + P U
         for (int t = grp; t < n; t += G) {
-            const float4* qt = reinterpret_cast<const float4*>(rec + R::Q + t * D);
-            const float* pt = rec + R::P + t * 64;
+            const float4* qt = reinterpret_cast<const float4*>(sQ + t * D);
+            const float* pt = sP + t * 64;
             float acc = 0.f;
 #pragma unroll
             for (int c4 = 0; c4 < D / 4; ++c4) {
@@ -295,8 +316,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_recur_kernel(ChunkLaunch p)
         __syncthreads();                                         // every read of S done
         // S <- Diag(gamma) S + Kbar^T U
         for (int c = grp; c < D; c += G) {
-            float acc = rec[R::G + c] * S[c * JB + jl];
-            for (int t = 0; t < n; ++t) acc = fmaf(rec[R::K + t * D + c], U[t * JB + jl], acc);
+            float acc = sG[c] * S[c * JB + jl];
+            for (int t = 0; t < n; ++t) acc = fmaf(sK[t * D + c], U[t * JB + jl], acc);
             S[c * JB + jl] = acc;
         }
         // a snapshot after this chunk
@@ -341,7 +362,8 @@ cudaError_t launch_simt_pair(const ChunkLaunch& p, cudaStream_t s, bool local) {
     }
     const int64_t chains = (int64_t)p.a.n_seqs * p.a.n_heads;
     if (chains == 0) return cudaSuccess;
-    const size_t smem = (size_t)(D * kSimtCols + 64 * kSimtCols) * sizeof(float);
+    const size_t smem = (size_t)(D * kSimtCols + 64 * kSimtCols + 3 * 64 * D + 64 * 64 + D + 64 * kSimtCols) *
+                        sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(simt_recur_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

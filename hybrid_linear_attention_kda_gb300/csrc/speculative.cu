@@ -21,6 +21,7 @@
 // over the state rows stay inside warps: its token loop has no CTA barrier.  All candidate tokens' inputs are staged in
 // shared memory next to the state load, so the token loop waits on no global
 // load.
+#include "async_copy.cuh"
 #include "kda_common.cuh"
 
 namespace kda {
@@ -184,15 +185,6 @@ __host__ __device__ constexpr size_t commit_smem(int T) {
     return (size_t)T * 3 * D * sizeof(float);
 }
 
-// A 16-byte asynchronous copy from global to shared memory: no register holds
-// the data, so a thread's copies are all in flight at once.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
-                 "l"(__cvta_generic_to_global(gmem))
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 template <typename T, int D, int NT>
 __global__ void __launch_bounds__(NT) commit_kernel(SpecLaunch p) {
